@@ -1,0 +1,148 @@
+"""ctypes binding over libattn.so (the C-ABI in include/attn.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the launch stream, and non-zero status codes become
+``AttnError``.  Every step of the computation runs in the library's kernels.
+The library is loaded on first use; if it is missing or cannot be loaded the
+call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libattn.so"
+_lock = threading.Lock()
+_lib = None
+
+# The symbols include/attn.h declares (checked by the CPU test-suite).
+EXPORTS = (
+    "attn_fwd",
+    "attn_fwd_visited",
+    "attn_check",
+    "attn_strerror",
+    "attn_tile_shape",
+    "attn_set_wait_timeout_ns",
+    "attn_debug_inject",
+    "attn_version",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_strerror(status)} ({status})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def library():
+    """Load libattn.so (built in-tree by __graft_entry__.build()); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(
+                f"{path} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fwd_args = [p, p, p, p, p, p, i, i, i, i, i, i, f, i, p]
+        lib.attn_fwd.argtypes = fwd_args
+        lib.attn_fwd.restype = i
+        lib.attn_fwd_visited.argtypes = fwd_args + [p]
+        lib.attn_fwd_visited.restype = i
+        lib.attn_check.argtypes = [p]
+        lib.attn_check.restype = i
+        lib.attn_strerror.argtypes = [i]
+        lib.attn_strerror.restype = ctypes.c_char_p
+        lib.attn_tile_shape.argtypes = [i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.attn_tile_shape.restype = i
+        lib.attn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.attn_set_wait_timeout_ns.restype = i
+        lib.attn_debug_inject.argtypes = [i]
+        lib.attn_debug_inject.restype = i
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = i
+        _lib = lib
+        return lib
+
+
+def attn_strerror(status: int) -> str:
+    return library().attn_strerror(int(status)).decode()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; fp16 or bf16 expected")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(fn, q, k, v, o, lse, mask_bits, causal, scale, stream, extra=()):
+    """q/o: [B,Hq,S,d]; k/v: [B,Hkv,S,d]; lse: fp32 [B,Hq,S] or None;
+    mask_bits: int32/uint32 [B,S,ceil(S/32)] or None.  Shapes are taken from q and k."""
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(mask_bits), int(B), int(Hq), int(Hkv),
+            int(S), int(d), int(bool(causal)), ctypes.c_float(scale), _dtype_code(q), _stream_handle(stream),
+            *extra)
+    if rc != 0:
+        raise AttnError(rc, fn.__name__)
+
+
+def attn_fwd(q, k, v, o, lse=None, mask_bits=None, causal=False, scale=None, stream=None):
+    """Launch the fused forward on `stream` (default: torch's current stream).
+
+    The caller owns every tensor (device memory, contiguous, [B,H,S,d]); the
+    call is asynchronous; use attn_check() to collect in-kernel errors."""
+    lib = library()
+    _call(lib.attn_fwd, q, k, v, o, lse, mask_bits, causal, scale, stream)
+
+
+def attn_fwd_visited(q, k, v, o, lse, mask_bits, causal, scale, visited, stream=None):
+    """attn_fwd that also sets visited[b, hq, qtile, ktile] = 1 (uint8) for every
+    (query tile, key tile) block the kernel computed; the caller zeroes it first."""
+    lib = library()
+    _call(lib.attn_fwd_visited, q, k, v, o, lse, mask_bits, causal, scale, stream, extra=(_ptr(visited),))
+
+
+def attn_check(stream=None) -> int:
+    """Synchronise `stream` and return the library status (0 = OK); raises on error."""
+    rc = library().attn_check(_stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_check")
+    return rc
+
+
+def attn_tile_shape(d: int):
+    """(rows per query tile, columns per key tile) the kernel uses for head dim d."""
+    bm, bn = ctypes.c_int(0), ctypes.c_int(0)
+    rc = library().attn_tile_shape(int(d), ctypes.byref(bm), ctypes.byref(bn))
+    if rc != 0:
+        raise AttnError(rc, "attn_tile_shape")
+    return bm.value, bn.value

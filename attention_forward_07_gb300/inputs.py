@@ -1,0 +1,147 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module only draws random numbers and packs them into the library's input
+formats; it holds none of the attention arithmetic.  Both the CUDA path and the
+fp64 oracle consume what it produces.
+
+Recipe (the workloads of the pages' benchmarks, all synthetic):
+
+* Q, K, V ~ N(0, 1) in float32 from ``torch.Generator('cpu').manual_seed(seed)``,
+  rounded to fp16 / bf16, laid out ``[B, H, S, d]``;
+* custom masks are drawn from a second generator seeded ``seed + 1``;
+  ``bernoulli_mask`` keeps each (b, row, col) with probability ``p_keep``;
+  ``block_sparse_mask`` zeroes whole 16-row blocks with probability 0.8 and
+  fills the others Bernoulli(0.5), for an expected masked fraction of 0.9;
+* masks are packed least-significant bit first into uint32 words
+  ``[B, S, ceil(S/32)]``, one word per 32 columns, 1 = attend, shared by every
+  head of a batch entry.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+F16, BF16 = 0, 1
+TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
+DTYPE_NAME = {F16: "f16", BF16: "bf16"}
+
+
+def qkv(B, Hq, Hkv, S, d, dtype, seed):
+    """Q [B,Hq,S,d], K and V [B,Hkv,S,d], N(0,1) rounded to fp16/bf16, on the CPU."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    dt = TORCH_DTYPE[dtype]
+    q = torch.randn((B, Hq, S, d), generator=g, dtype=torch.float32).to(dt)
+    k = torch.randn((B, Hkv, S, d), generator=g, dtype=torch.float32).to(dt)
+    v = torch.randn((B, Hkv, S, d), generator=g, dtype=torch.float32).to(dt)
+    return q, k, v
+
+
+def bernoulli_mask(B, S, seed, p_keep=0.5):
+    """bool [B, S, S]: each entry kept with probability p_keep."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed) + 1)
+    return torch.rand((B, S, S), generator=g) < p_keep
+
+
+def block_sparse_mask(B, S, seed, block=16, p_zero=0.8, p_keep=0.5):
+    """bool [B, S, S]: each block of `block` rows is all-zero with probability p_zero,
+    otherwise Bernoulli(p_keep) per entry (expected masked fraction 0.9)."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed) + 1)
+    nblk = (S + block - 1) // block
+    zero = torch.rand((B, nblk), generator=g) < p_zero
+    m = torch.rand((B, S, S), generator=g) < p_keep
+    rows_zero = zero.repeat_interleave(block, dim=1)[:, :S]
+    m[rows_zero] = False
+    return m
+
+
+def pack_bits(mask):
+    """bool [B, S, S] -> uint32 [B, S, ceil(S/32)], bit (c % 32) of word c // 32 = mask[.., c]."""
+    m = np.asarray(mask.numpy() if isinstance(mask, torch.Tensor) else mask, dtype=bool)
+    B, R, C = m.shape
+    W = (C + 31) // 32
+    padded = np.zeros((B, R, W * 32), dtype=bool)
+    padded[:, :, :C] = m
+    by = np.packbits(padded, axis=-1, bitorder="little")
+    return np.ascontiguousarray(by).view("<u4").reshape(B, R, W).astype(np.uint32)
+
+
+def unpack_bits(words, S):
+    """Inverse of pack_bits: uint32 [B, R, W] -> bool [B, R, S]."""
+    w = np.ascontiguousarray(np.asarray(words, dtype="<u4"))
+    by = w.view(np.uint8)
+    bits = np.unpackbits(by, axis=-1, bitorder="little")
+    return bits[:, :, :S].astype(bool)
+
+
+def as_u16(t: torch.Tensor) -> np.ndarray:
+    """The raw 16-bit words of a CPU fp16/bf16 tensor as a uint16 numpy array."""
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def sample_rows(B, Hq, S, n_random, seed, fixed=(0, 1, 127, 128)):
+    """Flat row ids (b*Hq + hq)*S + i: for every (b, hq) the rows in `fixed` that exist,
+    row S-1, and n_random rows drawn from a seeded generator."""
+    rng = np.random.default_rng(int(seed) + 7)
+    ids = []
+    for bh in range(B * Hq):
+        rows = {r for r in fixed if r < S} | {S - 1}
+        if n_random > 0:
+            rows |= set(int(x) for x in rng.integers(0, S, size=n_random))
+        ids.extend(bh * S + r for r in sorted(rows))
+    return np.asarray(ids, dtype=np.int64)
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One benchmark configuration of the pages (shapes, dtype, mask kind)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    d: int
+    dtype: int
+    causal: bool
+    mask: str  # "none" | "bernoulli" | "block90"
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.d)))
+
+    def flops(self) -> float:
+        """4*B*Hq*S^2*d, halved for causal (the dense count, also for custom masks)."""
+        f = 4.0 * self.B * self.Hq * self.S * self.S * self.d
+        return f / 2 if self.causal else f
+
+    def seed(self, index: int) -> int:
+        return index * 1000 + self.S
+
+    def make(self, seed):
+        q, k, v = qkv(self.B, self.Hq, self.Hkv, self.S, self.d, self.dtype, seed)
+        if self.mask == "bernoulli":
+            bits = pack_bits(bernoulli_mask(self.B, self.S, seed))
+        elif self.mask == "block90":
+            bits = pack_bits(block_sparse_mask(self.B, self.S, seed))
+        else:
+            bits = None
+        return q, k, v, bits
+
+
+def _prefill(name, S, Hq, Hkv, causal):
+    return Workload(name, 32768 // S, Hq, Hkv, S, 128, BF16, causal, "none")
+
+
+WORKLOADS = {
+    "tiny_masked": Workload("tiny_masked", 1, 2, 2, 128, 64, F16, False, "bernoulli"),
+    "short_masked": Workload("short_masked", 16, 16, 16, 512, 64, F16, False, "bernoulli"),
+    "short_masked90": Workload("short_masked90", 16, 16, 16, 512, 64, F16, False, "block90"),
+}
+for _S in (4096, 8192, 16384, 32768):
+    WORKLOADS[f"mha_causal_S{_S}"] = _prefill(f"mha_causal_S{_S}", _S, 16, 16, True)
+    WORKLOADS[f"mha_S{_S}"] = _prefill(f"mha_S{_S}", _S, 16, 16, False)
+    for _hkv in (4, 8):
+        WORKLOADS[f"gqa{_hkv}_causal_S{_S}"] = _prefill(f"gqa{_hkv}_causal_S{_S}", _S, 32, _hkv, True)
+        WORKLOADS[f"gqa{_hkv}_S{_S}"] = _prefill(f"gqa{_hkv}_S{_S}", _S, 32, _hkv, False)

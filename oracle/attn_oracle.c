@@ -1,0 +1,243 @@
+/*
+ * attn_oracle.c -- plain, slow, fp64 CPU definition of masked attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness oracle that the CUDA
+ * path is checked against.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  It shares no code, header, table
+ * or helper with the CUDA library.
+ *
+ * What it computes (per batch b, query head hq, query row i):
+ *
+ *   The web page "NVIDIA让AI狂肝7天自己写算子" (yetianai.com/news/16520),
+ *   section on the FlashAttention lineage, states that tiling only avoids
+ *   storing the full attention matrix; the result is ordinary attention:
+ *
+ *       s_j   = scale * <q_i, k_j>                      (j = 0 .. S-1)
+ *       keep  = allowed(i, j)
+ *       m     = max_{kept j} s_j
+ *       w_j   = exp(s_j - m) for kept j, else 0
+ *       l     = sum_j w_j
+ *       O_i   = sum_j w_j v_j / l
+ *       LSE_i = m + ln(l)
+ *
+ *   The page "Opus 4.6 + AutoResearch驱动25轮迭代..." (yunpan.plus/t/19526),
+ *   second code excerpt (in-register mask + scale), defines the custom mask:
+ *   column c of row r is kept when bit (c % 32) of word c / 32 of that row's
+ *   mask words is 1, and the score is multiplied by the scale after Q.K^T.
+ *
+ * Readings taken where the pages are silent (stated once, used throughout):
+ *   - masked entries are excluded (weight exactly 0), and a row with no kept
+ *     column has O_i = 0 and LSE_i = -inf;
+ *   - causal keeps j <= i (queries and keys have the same length S);
+ *   - causal and a custom mask may both be given: their kept sets are ANDed;
+ *   - mask words are laid out [B][S][ceil(S/32)], shared by all heads,
+ *     least-significant bit first, bits past column S-1 ignored;
+ *   - GQA maps query head hq to key/value head hq / (Hq / Hkv);
+ *   - tensors are [B][H][S][d] row-major; LSE is the natural log.
+ *
+ * Inputs are the raw 16-bit fp16 / bf16 words; they are widened to double
+ * exactly (the oracle consumes the same rounded values the GPU gets).
+ * Everything after that is double precision, in the order written above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of an IEEE binary16 word. */
+static double widen_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 0x1f;
+    int man = h & 0x3ff;
+    double x;
+    if (ex == 0)
+        x = ldexp((double)man, -24);               /* subnormal: man * 2^-24 */
+    else if (ex == 31)
+        x = man ? NAN : INFINITY;
+    else
+        x = ldexp((double)(man | 0x400), ex - 25); /* 1.man * 2^(ex-15) */
+    return sign ? -x : x;
+}
+
+/* Exact widening of a bfloat16 word: the top half of a binary32. */
+static double widen_bf16(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double widen(uint16_t w, int dtype) { return dtype ? widen_bf16(w) : widen_f16(w); }
+
+/* Is key column j kept for query row i of batch b? */
+static int allowed(const uint32_t *mask_bits, int b, int i, int j, int S, int causal)
+{
+    if (causal && j > i)
+        return 0;
+    if (mask_bits) {
+        int64_t W = (S + 31) / 32;
+        uint32_t word = mask_bits[((int64_t)b * S + i) * W + j / 32];
+        if (((word >> (j % 32)) & 1u) == 0)
+            return 0;
+    }
+    return 1;
+}
+
+/* One output row, straight from the definition.  scores has room for S doubles. */
+static void one_row(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                    const uint32_t *mask_bits, int B, int Hq, int Hkv, int S, int d,
+                    int causal, double scale, int64_t row_id, double *o_row, double *lse,
+                    double *scores, unsigned char *keep)
+{
+    (void)B;
+    int64_t i = row_id % S;
+    int64_t bh = row_id / S;
+    int64_t hq = bh % Hq;
+    int64_t b = bh / Hq;
+    int64_t hkv = hq / (Hq / Hkv);
+    const uint16_t *qi = q + ((b * Hq + hq) * S + i) * d;
+    const uint16_t *kb = k + (b * Hkv + hkv) * (int64_t)S * d;
+    const uint16_t *vb = v + (b * Hkv + hkv) * (int64_t)S * d;
+
+    double m = -INFINITY;
+    int any = 0;
+    for (int64_t j = 0; j < S; j++) {
+        keep[j] = (unsigned char)allowed(mask_bits, (int)b, (int)i, (int)j, S, causal);
+        if (!keep[j])
+            continue;
+        double dot = 0.0;
+        for (int t = 0; t < d; t++)
+            dot += widen(qi[t], dtype) * widen(kb[j * d + t], dtype);
+        scores[j] = scale * dot;
+        if (scores[j] > m)
+            m = scores[j];
+        any = 1;
+    }
+    for (int t = 0; t < d; t++)
+        o_row[t] = 0.0;
+    if (!any) {
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < S; j++) {
+        if (!keep[j])
+            continue;
+        double w = exp(scores[j] - m);
+        l += w;
+        for (int t = 0; t < d; t++)
+            o_row[t] += w * widen(vb[j * d + t], dtype);
+    }
+    for (int t = 0; t < d; t++)
+        o_row[t] /= l;
+    *lse = m + log(l);
+}
+
+/*
+ * oracle_attn_rows: evaluate the definition on a list of flat row ids
+ * (row_id = (b * Hq + hq) * S + i).  o_out is [nrows][d], lse_out is [nrows].
+ * nthreads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                     const uint32_t *mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+                     double scale, const int64_t *rows, int64_t nrows, double *o_out,
+                     double *lse_out, int nthreads)
+{
+    if (!q || !k || !v || !rows || !o_out || !lse_out)
+        return -1;
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || d < 1 || Hq % Hkv != 0)
+        return -1;
+    int64_t total = (int64_t)B * Hq * S;
+    for (int64_t r = 0; r < nrows; r++)
+        if (rows[r] < 0 || rows[r] >= total)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)S);
+        unsigned char *keep = (unsigned char *)malloc((size_t)S);
+        if (!scores || !keep) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < nrows; r++)
+                one_row(q, k, v, dtype, mask_bits, B, Hq, Hkv, S, d, causal, scale, rows[r],
+                        o_out + r * d, lse_out + r, scores, keep);
+        }
+        free(scores);
+        free(keep);
+    }
+    return failed ? -2 : 0;
+}
+
+/* oracle_attn_fwd: every row.  o_out is [B][Hq][S][d], lse_out is [B][Hq][S]. */
+int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                    const uint32_t *mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+                    double scale, double *o_out, double *lse_out, int nthreads)
+{
+    int64_t total = (int64_t)B * Hq * S;
+    if (total < 1)
+        return -1;
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)total);
+    if (!rows)
+        return -2;
+    for (int64_t r = 0; r < total; r++)
+        rows[r] = r;
+    int rc = oracle_attn_rows(q, k, v, dtype, mask_bits, B, Hq, Hkv, S, d, causal, scale, rows,
+                              total, o_out, lse_out, nthreads);
+    free(rows);
+    return rc;
+}
+
+/*
+ * oracle_skip_map: which (query tile, key tile) blocks hold at least one kept
+ * entry.  A block is empty -- and a tiled kernel may skip it -- exactly when
+ * no (i, j) inside it is kept; blocks wholly above the causal diagonal are
+ * empty.  This is the tile-skip rule of the first page's ballot excerpt,
+ * evaluated for tiles of bm rows by bn columns.  out is [B][nqt][nkt] bytes,
+ * nqt = ceil(S/bm), nkt = ceil(S/bn); 1 = non-empty.
+ */
+int oracle_skip_map(const uint32_t *mask_bits, int B, int S, int causal, int bm, int bn,
+                    unsigned char *out)
+{
+    if (!out || B < 1 || S < 1 || bm < 1 || bn < 1)
+        return -1;
+    int nqt = (S + bm - 1) / bm, nkt = (S + bn - 1) / bn;
+    for (int b = 0; b < B; b++)
+        for (int qt = 0; qt < nqt; qt++)
+            for (int kt = 0; kt < nkt; kt++) {
+                int hit = 0;
+                for (int i = qt * bm; i < S && i < (qt + 1) * bm && !hit; i++)
+                    for (int j = kt * bn; j < S && j < (kt + 1) * bn; j++)
+                        if (allowed(mask_bits, b, i, j, S, causal)) {
+                            hit = 1;
+                            break;
+                        }
+                out[((int64_t)b * nqt + qt) * nkt + kt] = (unsigned char)hit;
+            }
+    return 0;
+}
+
+/* Exposed so the tests can check the widening against library conversions. */
+double oracle_widen(uint16_t w, int dtype) { return widen(w, dtype); }
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
