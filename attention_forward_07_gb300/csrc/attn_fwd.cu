@@ -1,0 +1,862 @@
+// attn_fwd.cu -- fused attention forward for GB300 (sm_103a) and the C-ABI of libattn.so.
+//
+// O = softmax(scale * Q K^T + mask) V and LSE, tile by tile with a running max and
+// running sum (the FlashAttention scheme of the page "NVIDIA让AI狂肝7天自己写算子",
+// FlashAttention-lineage section), so the S x S scores never leave the SM.
+//
+// One persistent CTA per SM, 384 threads, warp-specialised:
+//   warp 0       load warp: TMA loads of the two 128-row Q tiles of a work unit and of
+//                the K / V tiles into a ring of 128-byte-swizzled shared-memory slots;
+//                for custom masks it also stages the tile's mask words in shared memory
+//                and decides, with a warp ballot, which (Q tile, K tile) blocks hold a
+//                kept entry (the tile-skip ballot of the page "Opus 4.6 +
+//                AutoResearch驱动25轮迭代...", first excerpt).  Empty blocks are never
+//                loaded or computed.
+//   warp 1       MMA warp: one thread issues tcgen05.mma.  S_t = Q_t K^T (both operands in
+//                shared memory, fp32 accumulator in TMEM) and O_t += P_t V (P_t read from
+//                TMEM, V from shared memory), interleaved so the QK^T of the next key tile
+//                of a Q tile is queued right behind that tile's P.V.
+//   warps 4-7,   softmax warpgroups, one per Q tile, one thread per query row (= TMEM
+//   8-11         lane): load the 128 scores of the row, scale, mask (causal bound or
+//                staged bit words, as in the page's in-register mask excerpt), row max,
+//                exp2, row sum, write P back into TMEM as fp16/bf16, rescale the O row
+//                when the running max grew (the correction step), and at the end of the
+//                unit normalise O, store it and the LSE.
+// Work unit = (batch, query head, 256-row block); units are dealt to CTAs in a fixed
+// snake order; for causal masks the heaviest blocks (most key tiles) come first.
+// Every barrier wait is bounded: a wait that runs out sets a shared abort flag and the
+// device status word, every role drains what it has in flight and the CTA returns.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int BM = 128;        // query rows per Q tile = TMEM lanes
+constexpr int QT = 2;          // Q tiles per work unit
+constexpr int UNIT_ROWS = BM * QT;
+constexpr int BN = 128;        // keys per K/V tile
+constexpr int NTHREADS = 384;  // 12 warps
+constexpr int NINFO = 4;       // depth of the tile-descriptor ring
+constexpr int TMEM_COLS = 512;
+constexpr int S_COL0 = 0;      // S_t (fp32, 128 columns) at t*128; P_t aliases its first 64
+constexpr int O_COL0 = 256;    // O_t (fp32, d columns) at 256 + t*128
+constexpr int FLAG_END = 4;    // info entry marking the end of a work unit
+constexpr float LN2 = 0.69314718055994530942f;
+
+enum MaskMode { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_CUSTOM = 2 };
+
+template <int D, int MODE>
+struct Layout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int HALVES = D / 64;                  // 128-byte swizzle spans per row
+  static constexpr int Q_TILE_BYTES = BM * D * 2;
+  static constexpr int KV_TILE_BYTES = BN * D * 2;
+  static constexpr int NSLOT = (D == 128) ? (MODE == MASK_CUSTOM ? 4 : 5) : 8;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + QT * Q_TILE_BYTES;
+  static constexpr int OFF_WORDS = OFF_KV + NSLOT * KV_TILE_BYTES;
+  static constexpr int WORDS_PER_ENTRY = UNIT_ROWS * (BN / 32);
+  static constexpr int OFF_HDR = OFF_WORDS + (MODE == MASK_CUSTOM ? NINFO * WORDS_PER_ENTRY * 4 : 0);
+  static constexpr int OFF_BAR = OFF_HDR + NINFO * 16;
+  // barrier indices
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_SFULL = 2, B_SEMPTY = 2 + NSLOT,
+                       B_IFULL = 2 + 2 * NSLOT, B_IEMPTY = B_IFULL + NINFO,
+                       B_STILE = B_IEMPTY + NINFO, B_PREADY = B_STILE + QT,
+                       B_ODONE = B_PREADY + QT, B_DRAIN = B_ODONE + QT, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+  static_assert(SMEM_ALLOC <= 232448, "shared memory");
+  // Over half of the SM's shared memory: one CTA per SM, so TMEM (512 columns) never
+  // has to be shared between resident CTAs.
+  static_assert(SMEM_ALLOC > 116 * 1024, "one CTA per SM");
+};
+
+struct InfoHdr {
+  int j;      // key tile index
+  int flags;  // bit t: Q tile t computes this key tile; FLAG_END: end of unit
+  int pad[2];
+};
+
+struct Params {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps {d, S, B*H}, box {64, 128, 1}, 128B swizzle
+  void* o;
+  float* lse;
+  const uint32_t* mask;
+  uint8_t* visited;
+  int B, Hq, Hkv, S, g, nqb, nkt, nqt, W, num_units;
+  int causal;
+  int inject;
+  float scale_log2;
+  unsigned long long timeout_ns;
+};
+
+}  // namespace attn
+
+// Device status word: bit 0 = a barrier wait ran out of time.
+__device__ unsigned int g_attn_status;
+
+namespace attn {
+
+// Slow path of a bounded barrier wait.  Gives up when another thread has aborted, when
+// the wait has lasted timeout_ns, or after an iteration cap, and then aborts the CTA.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       unsigned long long timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 28); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > timeout_ns) break;
+  }
+  *abort_flag = 1;
+  atomicOr(&g_attn_status, 1u);
+  return false;
+}
+
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, timeout_ns);
+}
+
+// Warp-uniform variant: every lane waits, and the warp only proceeds if all lanes did.
+__device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned long long timeout_ns) {
+  bool ok = bwait(bar, parity, abort_flag, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used only while draining after an abort: ignores the abort flag, short limit.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > 200000000ull) return;
+  }
+}
+
+// k-th unit of this CTA in the snake order, or -1 when it has none left.
+__device__ __forceinline__ int unit_at(int k, int num_units) {
+  const int G = gridDim.x;
+  const int u = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return u < num_units ? u : -1;
+}
+
+// Unit -> (batch, query head, 256-row block).  Causal: block index descending (the
+// longest units first), heads of a block adjacent.  Otherwise: consecutive units walk
+// the blocks and the heads of one K/V head, so concurrent CTAs share K/V through L2.
+__device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, int& b, int& hq,
+                                            int& qb) {
+  if (causal) {
+    const int bh = u % (p.B * p.Hq);
+    qb = p.nqb - 1 - u / (p.B * p.Hq);
+    b = bh / p.Hq;
+    hq = bh % p.Hq;
+  } else {
+    const int member = u % p.g;
+    const int rest = u / p.g;
+    qb = rest % p.nqb;
+    const int bk = rest / p.nqb;
+    const int hkv = bk % p.Hkv;
+    b = bk / p.Hkv;
+    hq = hkv * p.g + member;
+  }
+}
+
+// Last query row (inclusive, clipped to S-1) of Q tile t of block qb.
+__device__ __forceinline__ int last_row(int qb, int t, int S) {
+  return min(qb * UNIT_ROWS + t * BM + BM - 1, S - 1);
+}
+
+}  // namespace attn
+
+namespace attn {
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// ------------------------------------------------------------------ load warp (warp 0)
+template <int D, bool BF16, int MODE>
+__device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_t* gbase,
+                                          volatile int* abort_flag, int lane) {
+  using L = Layout<D, MODE>;
+  const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
+  const unsigned long long to = p.timeout_ns;
+  const uint32_t bars = base + L::OFF_BAR;
+  uint32_t* words = reinterpret_cast<uint32_t*>(gbase + L::OFF_WORDS);
+  volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
+
+  uint32_t q_empty_par = 1;     // producer waits on "empty" barriers starting from parity 1
+  uint32_t q_fills = 0;         // Q loads issued so far
+  int slot = 0;
+  uint32_t slot_par = 1;
+  uint32_t pend_mask = 0, pend_par = 0;  // slots with a load issued, and its full-barrier parity
+  int ie = 0;
+  uint32_t ie_par = 1;
+  bool inject = p.inject != 0;
+
+  for (int k = 0;; ++k) {
+    const int u = unit_at(k, p.num_units);
+    if (u < 0) break;
+    int b, hq, qb;
+    decode_unit(u, p, causal, b, hq, qb);
+    const int hkv = hq / p.g;
+    const int row0 = qb * UNIT_ROWS;
+
+    // Both Q tiles of the unit (rows past S are zero-filled by the TMA unit).
+    if (!bwait_warp(bars + 8u * L::B_QEMPTY, q_empty_par, abort_flag, to)) goto drain;
+    q_empty_par ^= 1u;
+    if (!inject) {
+      if (lane == 0) {
+        const uint32_t fb = bars + 8u * L::B_QFULL;
+        mbar_expect_tx(fb, QT * L::Q_TILE_BYTES);
+#pragma unroll
+        for (int t = 0; t < QT; ++t)
+#pragma unroll
+          for (int h = 0; h < L::HALVES; ++h)
+            tma_load_3d(base + L::OFF_Q + t * L::Q_TILE_BYTES + h * BM * 128, &p.tm_q, fb, h * 64,
+                        row0 + t * BM, b * p.Hq + hq);
+      }
+      ++q_fills;
+    }
+    inject = false;
+
+    const int jend = causal ? (last_row(qb, QT - 1, p.S) / BN + 1) : p.nkt;
+    for (int j = 0; j < jend; ++j) {
+      bool a0 = true;
+      bool a1 = (row0 + BM) < p.S;
+      if (causal) {
+        a0 = j * BN <= last_row(qb, 0, p.S);
+        a1 = a1 && (j * BN <= last_row(qb, 1, p.S));
+      }
+      uint32_t w[32];
+      if constexpr (MODE == MASK_CUSTOM) {
+        // Kept-bit words of the 256 rows x 4 words of this block: the custom mask ANDed with
+        // the causal bound and the key bound.  Lane l handles word (it*32 + l): row
+        // (it*32 + l) / 4, word (it*32 + l) % 4 -- coalesced 16-byte row segments.
+        uint32_t or0 = 0, or1 = 0;
+#pragma unroll
+        for (int it = 0; it < 32; ++it) {
+          const int idx = it * 32 + lane;
+          const int i = row0 + (idx >> 2);
+          const int gw = j * (BN / 32) + (idx & 3);
+          uint32_t x = 0;
+          if (i < p.S && gw < p.W) {
+            x = __ldg(p.mask + ((size_t)b * p.S + i) * p.W + gw);
+            const int nvalid = p.S - gw * 32;
+            if (nvalid < 32) x &= (1u << nvalid) - 1u;
+            if (causal) {
+              const int lim = i - gw * 32 + 1;
+              x = lim <= 0 ? 0u : (lim < 32 ? (x & ((1u << lim) - 1u)) : x);
+            }
+          }
+          w[it] = x;
+          if (it < 16) or0 |= x; else or1 |= x;
+        }
+        const bool any0 = __any_sync(0xffffffffu, or0 != 0u);
+        const bool any1 = __any_sync(0xffffffffu, or1 != 0u);
+        a0 = a0 && any0;
+        a1 = a1 && any1;
+      }
+      if (!a0 && !a1) continue;  // empty block pair: nothing loaded, nothing computed
+
+      if (!bwait_warp(bars + 8u * (L::B_IEMPTY + ie), ie_par, abort_flag, to)) goto drain;
+      if constexpr (MODE == MASK_CUSTOM) {
+        uint32_t* dst = words + ie * L::WORDS_PER_ENTRY;
+#pragma unroll
+        for (int it = 0; it < 32; ++it) dst[it * 32 + lane] = w[it];
+      }
+      if (lane == 0) {
+        hdr[ie].j = j;
+        hdr[ie].flags = (a0 ? 1 : 0) | (a1 ? 2 : 0);
+      }
+      __syncwarp();
+      mbar_arrive(bars + 8u * (L::B_IFULL + ie));
+      if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
+
+      for (int kv = 0; kv < 2; ++kv) {  // K tile, then V tile
+        if (!bwait_warp(bars + 8u * (L::B_SEMPTY + slot), slot_par, abort_flag, to)) goto drain;
+        if (lane == 0) {
+          const uint32_t fb = bars + 8u * (L::B_SFULL + slot);
+          mbar_expect_tx(fb, L::KV_TILE_BYTES);
+#pragma unroll
+          for (int h = 0; h < L::HALVES; ++h)
+            tma_load_3d(base + L::OFF_KV + slot * L::KV_TILE_BYTES + h * BN * 128,
+                        kv ? (const void*)&p.tm_v : (const void*)&p.tm_k, fb, h * 64, j * BN,
+                        b * p.Hkv + hkv);
+        }
+        pend_mask |= 1u << slot;
+        pend_par = (pend_par & ~(1u << slot)) | ((slot_par ^ 1u) << slot);
+        if (++slot == L::NSLOT) { slot = 0; slot_par ^= 1u; }
+      }
+    }
+    // End-of-unit marker.
+    if (!bwait_warp(bars + 8u * (L::B_IEMPTY + ie), ie_par, abort_flag, to)) goto drain;
+    if (lane == 0) {
+      hdr[ie].j = -1;
+      hdr[ie].flags = FLAG_END;
+    }
+    __syncwarp();
+    mbar_arrive(bars + 8u * (L::B_IFULL + ie));
+    if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
+  }
+  return;
+
+drain:
+  // Aborted: let the copies this warp started land before the CTA exits.
+  if (lane == 0) {
+    for (int s = 0; s < L::NSLOT; ++s)
+      if ((pend_mask >> s) & 1u) wait_drain(bars + 8u * (L::B_SFULL + s), (pend_par >> s) & 1u);
+    if (q_fills > 0) wait_drain(bars + 8u * L::B_QFULL, (q_fills - 1u) & 1u);
+  }
+  __syncwarp();
+}
+
+}  // namespace attn
+
+namespace attn {
+
+// ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
+// Per tile descriptor e (key tile j) and Q tile t, in this order:
+//   O_t (+)= P_t(prev) . V(prev)    once softmax t has written P for the previous tile
+//   S_t     = Q_t . K(j)^T          then signal softmax t
+// so S_t / P_t (which share TMEM columns) are rewritten only after the P.V that reads them.
+template <int D, bool BF16, int MODE>
+__device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t* gbase,
+                                         volatile int* abort_flag, uint32_t tmem) {
+  using L = Layout<D, MODE>;
+  const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
+  const unsigned long long to = p.timeout_ns;
+  const uint32_t bars = base + L::OFF_BAR;
+  volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
+  constexpr uint32_t ID_QK = idesc_f16acc32(BF16, false, false, BM, BN);
+  constexpr uint32_t ID_PV = idesc_f16acc32(BF16, false, true, BM, D);
+
+  uint32_t q_par = 0, ie_par = 0, slot_par = 0, p_par0 = 0, p_par1 = 0;
+  int slot = 0, ie = 0;
+
+  for (int k = 0;; ++k) {
+    const int u = unit_at(k, p.num_units);
+    if (u < 0) break;
+    int b, hq, qb;
+    decode_unit(u, p, causal, b, hq, qb);
+    if (!bwait(bars + 8u * L::B_QFULL, q_par, abort_flag, to)) goto drain;
+    q_par ^= 1u;
+    tc_fence_after();
+
+    bool have_prev = false, pv0 = false, pv1 = false;
+    int prev_flags = 0, prev_vslot = 0;
+    uint32_t prev_vpar = 0;
+    while (true) {
+      if (!bwait(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) goto drain;
+      const int j = hdr[ie].j;
+      const int flags = hdr[ie].flags;
+      const bool end = (flags & FLAG_END) != 0;
+      int kslot = 0, vslot = 0;
+      uint32_t vpar = 0;
+      if (!end) {
+        kslot = slot;
+        const uint32_t kpar = slot_par;
+        if (++slot == L::NSLOT) { slot = 0; slot_par ^= 1u; }
+        vslot = slot;
+        vpar = slot_par;
+        if (++slot == L::NSLOT) { slot = 0; slot_par ^= 1u; }
+        if (!bwait(bars + 8u * (L::B_SFULL + kslot), kpar, abort_flag, to)) goto drain;
+      }
+      if (have_prev && !bwait(bars + 8u * (L::B_SFULL + prev_vslot), prev_vpar, abort_flag, to))
+        goto drain;
+      tc_fence_after();
+
+#pragma unroll
+      for (int t = 0; t < QT; ++t) {
+        const uint32_t s_col = tmem + S_COL0 + t * 128;
+        if (have_prev && ((prev_flags >> t) & 1)) {
+          uint32_t& pp = t ? p_par1 : p_par0;
+          if (!bwait(bars + 8u * (L::B_PREADY + t), pp, abort_flag, to)) goto drain;
+          pp ^= 1u;
+          tc_fence_after();
+          bool& started = t ? pv1 : pv0;
+          const uint32_t vbase = base + L::OFF_KV + prev_vslot * L::KV_TILE_BYTES;
+          // V tile as the MN-major B operand: 16 keys per step (2048 bytes), the two
+          // 64-column halves of d are KV_TILE_BYTES/2 apart, 8-key groups 1024 apart.
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + O_COL0 + t * 128, s_col + kk * 8,
+                   sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
+                   (started || kk > 0) ? 1u : 0u);
+          started = true;
+        }
+        if (!end && ((flags >> t) & 1)) {
+          const uint32_t qbase = base + L::OFF_Q + t * L::Q_TILE_BYTES;
+          const uint32_t kbase = base + L::OFF_KV + kslot * L::KV_TILE_BYTES;
+          // Q and K as K-major operands: 16 elements (32 bytes) per step inside a
+          // 128-byte swizzle row, the next 64 elements one half-tile further.
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+            mma_ss(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                   ID_QK, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bars + 8u * (L::B_STILE + t));
+          if (p.visited)
+            p.visited[((size_t)(b * p.Hq + hq) * p.nqt + (qb * QT + t)) * p.nkt + j] = 1;
+        }
+      }
+      if (have_prev) tc_commit(bars + 8u * (L::B_SEMPTY + prev_vslot));
+      if (!end) tc_commit(bars + 8u * (L::B_SEMPTY + kslot));
+      mbar_arrive(bars + 8u * (L::B_IEMPTY + ie));
+      if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
+      if (end) break;
+      have_prev = true;
+      prev_flags = flags;
+      prev_vslot = vslot;
+      prev_vpar = vpar;
+    }
+    if (pv0) tc_commit(bars + 8u * (L::B_ODONE + 0));
+    if (pv1) tc_commit(bars + 8u * (L::B_ODONE + 1));
+    tc_commit(bars + 8u * L::B_QEMPTY);
+  }
+  return;
+
+drain:
+  // Aborted: wait until every MMA this thread issued has finished before TMEM is freed.
+  tc_commit(bars + 8u * L::B_DRAIN);
+  wait_drain(bars + 8u * L::B_DRAIN, 0);
+}
+
+}  // namespace attn
+
+namespace attn {
+
+// ------------------------------------------------------------------ softmax warpgroup t
+// Thread r of the warpgroup owns query row qb*256 + t*128 + r, i.e. TMEM lane r.
+// Running state in the exp2 domain: m = max of scale*log2(e)*s over the kept keys seen
+// so far, l = sum of 2^(scale*log2(e)*s - m).  LSE = ln2 * (m + log2 l).
+template <int D, bool BF16, int MODE>
+__device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uint8_t* gbase,
+                                             volatile int* abort_flag, uint32_t tmem, int t,
+                                             int quarter, int lane) {
+  using L = Layout<D, MODE>;
+  using OutT = uint16_t;
+  const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
+  const unsigned long long to = p.timeout_ns;
+  const uint32_t bars = base + L::OFF_BAR;
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(gbase + L::OFF_WORDS);
+  volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
+  const int r = quarter * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+  const uint32_t s_addr = tmem + lane_off + S_COL0 + t * 128;
+  const uint32_t o_addr = tmem + lane_off + O_COL0 + t * 128;
+  const float c = p.scale_log2;
+
+  uint32_t s_par = 0, o_par = 0, ie_par = 0;
+  int ie = 0;
+
+  for (int k = 0;; ++k) {
+    const int u = unit_at(k, p.num_units);
+    if (u < 0) break;
+    int b, hq, qb;
+    decode_unit(u, p, causal, b, hq, qb);
+    const int i = qb * UNIT_ROWS + t * BM + r;
+    float m = -INFINITY, l = 0.f;
+    int nact = 0;
+
+    while (true) {
+      if (!bwait_warp(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) return;
+      const int j = hdr[ie].j;
+      const int flags = hdr[ie].flags;
+      const bool end = (flags & FLAG_END) != 0;
+      const bool act = !end && ((flags >> t) & 1);
+      uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (MODE == MASK_CUSTOM) {
+        if (act) wv = *reinterpret_cast<const uint4*>(words + ie * L::WORDS_PER_ENTRY + (t * BM + r) * 4);
+      }
+      mbar_arrive(bars + 8u * (L::B_IEMPTY + ie));
+      if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
+      if (end) break;
+      if (!act) continue;
+
+      if (!bwait_warp(bars + 8u * (L::B_STILE + t), s_par, abort_flag, to)) return;
+      s_par ^= 1u;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld32x32b_x128_wait(s_addr, sr);
+
+      // Mask: excluded scores become -inf (weight exactly 0).
+      if constexpr (MODE == MASK_CUSTOM) {
+        const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc)
+          if (!((wa[cc >> 5] >> (cc & 31)) & 1u)) sr[cc] = __float_as_uint(-INFINITY);
+      } else {
+        int lim = p.S - j * BN;  // keys at or past S
+        if (MODE == MASK_CAUSAL) lim = min(lim, i - j * BN + 1);
+        if (__any_sync(0xffffffffu, lim < BN)) {
+#pragma unroll
+          for (int cc = 0; cc < 128; ++cc)
+            if (cc >= lim) sr[cc] = __float_as_uint(-INFINITY);
+        }
+      }
+
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 128; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
+      const float m_new = fmaxf(m, mx * c);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+
+      // Correction: rescale this row of O when its running max grew.
+      if (nact > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t ob[32];
+          tmem_ld32x32b_x32_wait(o_addr + ch * 32, ob);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ob[x] = __float_as_uint(__uint_as_float(ob[x]) * alpha);
+          tmem_st32x32b_x32(o_addr + ch * 32, ob);
+        }
+      }
+
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int cc = 0; cc < 64; ++cc) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
+        sum += p0 + p1;
+        pk[cc] = pack2<BF16>(p0, p1);
+      }
+      tmem_st32x32b_x64(s_addr, pk);  // P_t over the first 64 columns of S_t
+      tmem_wait_st();
+      l = l * alpha + sum;
+      m = m_new;
+      tc_fence_before();
+      mbar_arrive(bars + 8u * (L::B_PREADY + t));
+      ++nact;
+    }
+
+    // Epilogue: O = O_acc / l, LSE; rows with nothing kept give O = 0, LSE = -inf.
+    if (nact > 0) {
+      if (!bwait_warp(bars + 8u * (L::B_ODONE + t), o_par, abort_flag, to)) return;
+      o_par ^= 1u;
+      tc_fence_after();
+    }
+    const bool row_ok = i < p.S;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.S + (row_ok ? i : 0)) * D;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t ob[32];
+      if (nact > 0) {
+        tmem_ld32x32b_x32_wait(o_addr + ch * 32, ob);
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) ob[x] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int x = 0; x < 16; ++x)
+        pk[x] = pack2<BF16>(__uint_as_float(ob[2 * x]) * inv, __uint_as_float(ob[2 * x + 1]) * inv);
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
+    }
+    if (row_ok && p.lse)
+      p.lse[(size_t)(b * p.Hq + hq) * p.S + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int D, bool BF16, int MODE>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_constant__ Params p) {
+  using L = Layout<D, MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte tiles
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bars = base + L::OFF_BAR;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars + 8u * L::B_QFULL, 1);
+    mbar_init(bars + 8u * L::B_QEMPTY, 1);
+    for (int s = 0; s < L::NSLOT; ++s) {
+      mbar_init(bars + 8u * (L::B_SFULL + s), 1);
+      mbar_init(bars + 8u * (L::B_SEMPTY + s), 1);
+    }
+    for (int e = 0; e < NINFO; ++e) {
+      mbar_init(bars + 8u * (L::B_IFULL + e), 32);                // the whole load warp
+      mbar_init(bars + 8u * (L::B_IEMPTY + e), 1 + QT * BM);      // MMA thread + softmax threads
+    }
+    for (int t = 0; t < QT; ++t) {
+      mbar_init(bars + 8u * (L::B_STILE + t), 1);
+      mbar_init(bars + 8u * (L::B_PREADY + t), BM);
+      mbar_init(bars + 8u * (L::B_ODONE + t), 1);
+    }
+    mbar_init(bars + 8u * L::B_DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.tm_q);
+    tma_prefetch_map(&p.tm_k);
+    tma_prefetch_map(&p.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    load_role<D, BF16, MODE>(p, base, gbase, abort_flag, lane);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem);
+    __syncwarp();
+  } else if (warp >= 4) {
+    softmax_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem, (warp - 4) >> 2, warp & 3, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace attn
+
+// ====================================================================== host side
+namespace attn {
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_inject{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  int state = 0;  // 0 unknown, 1 usable, -1 not an sm_103 device
+  int sms = 0;
+};
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+int device_info(int& sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  DeviceInfo& di = g_dev[dev];
+  if (di.state == 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_DEVICE;
+    di.state = (major == 10 && minor == 3) ? 1 : -1;
+    di.sms = n;
+  }
+  if (di.state != 1) return ATTN_ERR_DEVICE;
+  sms = di.sms;
+  return ATTN_OK;
+}
+
+// [rows = B*H][S][d] tensor as a 3-D map {d, S, B*H}; box {64, 128, 1}: one 128-byte
+// swizzle span of 128 rows.  Rows past S read as zeros.
+int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long BH) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool BF16, int MODE>
+int launch(const Params& p, int grid, cudaStream_t st) {
+  using L = Layout<D, MODE>;
+  auto kern = attn_fwd_kernel<D, BF16, MODE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  kern<<<grid, NTHREADS, L::SMEM_ALLOC, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool BF16>
+int launch_mode(const Params& p, int mode, int grid, cudaStream_t st) {
+  switch (mode) {
+    case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st);
+    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st);
+    default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st);
+  }
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+             const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+             float scale, int dtype, void* stream, uint8_t* visited) {
+  // ---- validation (no CUDA call before this block is passed)
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID;
+  const uintptr_t a16 = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)o;
+  if (a16 & 15u) return ATTN_ERR_INVALID;
+  if (((uintptr_t)lse & 3u) || ((uintptr_t)mask_bits & 3u)) return ATTN_ERR_INVALID;
+  const long long nqb = (S + UNIT_ROWS - 1) / UNIT_ROWS;
+  if ((long long)B * Hq * S > INT_MAX || (long long)B * Hq * nqb > INT_MAX) return ATTN_ERR_INVALID;
+
+  int sms = 0;
+  int rc = device_info(sms);
+  if (rc != ATTN_OK) return rc;
+
+  Params p;
+  std::memset(&p, 0, sizeof p);
+  const bool bf16 = dtype == ATTN_BF16;
+  if ((rc = make_map(&p.tm_q, q, bf16, d, S, (long long)B * Hq)) != ATTN_OK) return rc;
+  if ((rc = make_map(&p.tm_k, k, bf16, d, S, (long long)B * Hkv)) != ATTN_OK) return rc;
+  if ((rc = make_map(&p.tm_v, v, bf16, d, S, (long long)B * Hkv)) != ATTN_OK) return rc;
+  p.o = o;
+  p.lse = lse;
+  p.mask = mask_bits;
+  p.visited = visited;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.g = Hq / Hkv;
+  p.nqb = (int)nqb;
+  p.nkt = (S + BN - 1) / BN;
+  p.nqt = (S + BM - 1) / BM;
+  p.W = (S + 31) / 32;
+  p.num_units = B * Hq * (int)nqb;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns.load();
+  p.inject = g_inject.exchange(0);
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  const int mode = mask_bits ? MASK_CUSTOM : (causal ? MASK_CAUSAL : MASK_NONE);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 64)
+    return bf16 ? launch_mode<64, true>(p, mode, grid, st) : launch_mode<64, false>(p, mode, grid, st);
+  return bf16 ? launch_mode<128, true>(p, mode, grid, st) : launch_mode<128, false>(p, mode, grid, st);
+}
+
+}  // namespace
+}  // namespace attn
+
+// ====================================================================== C-ABI
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+             float scale, int dtype, void* stream) {
+  return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
+                        nullptr);
+}
+
+int attn_fwd_visited(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+                     float scale, int dtype, void* stream, uint8_t* visited) {
+  if (!visited) return ATTN_ERR_INVALID;
+  return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
+                        visited);
+}
+
+int attn_check(void* stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  unsigned int status = 0;
+  if (cudaMemcpyFromSymbol(&status, g_attn_status, sizeof status) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (status != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+const char* attn_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dim or dtype";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case ATTN_ERR_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int attn_tile_shape(int d, int* bm, int* bn) {
+  if (!bm || !bn) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  *bm = attn::BM;
+  *bn = attn::BN;
+  return ATTN_OK;
+}
+
+int attn_set_wait_timeout_ns(unsigned long long ns) {
+  attn::g_timeout_ns.store(ns ? ns : attn::kDefaultTimeoutNs);
+  return ATTN_OK;
+}
+
+int attn_debug_inject(int flag) {
+  if (flag != 0 && flag != 1) return ATTN_ERR_INVALID;
+  attn::g_inject.store(flag);
+  return ATTN_OK;
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+"""Helpers shared by the GPU tests: run the CUDA path through the C-ABI, compare to the oracle."""
+import numpy as np
+import torch
+
+import attention_forward_07_gb300 as af
+import oracle
+from attention_forward_07_gb300 import inputs as inp
+
+O_ATOL, O_RTOL, LSE_ATOL = 1e-2, 1e-2, 1e-3
+
+
+def run_cuda(q, k, v, bits, causal, scale, visited=False, dev="cuda:0"):
+    """Copy CPU inputs to the device, run attn_fwd (or attn_fwd_visited), return host results."""
+    B, Hq, S, d = q.shape
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if bits is None else torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device=dev)
+    vis = None
+    if visited:
+        bm, bn = af.attn_tile_shape(d)
+        vis = torch.zeros((B, Hq, -(-S // bm), -(-S // bn)), dtype=torch.uint8, device=dev)
+        af.attn_fwd_visited(qd, kd, vd, o, lse, md, causal, scale, vis)
+    else:
+        af.attn_fwd(qd, kd, vd, o, lse, md, causal=causal, scale=scale)
+    af.attn_check()
+    out = (o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
+    if visited:
+        out = out + (vis.cpu().numpy(),)
+    return out
+
+
+def oracle_full(q, k, v, bits, causal, scale, dtype):
+    return oracle.attn_fwd(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), dtype, bits, causal,
+                           float(np.float32(scale)))
+
+
+def oracle_rows(q, k, v, bits, causal, scale, dtype, rows):
+    return oracle.attn_rows(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), dtype, rows, bits, causal,
+                            float(np.float32(scale)))
+
+
+def assert_close(o, lse, o_ref, lse_ref, what=""):
+    """The parity bar: |O - O_ref| <= 1e-2 + 1e-2*|O_ref| elementwise, |LSE - LSE_ref| <= 1e-3,
+    -inf LSE exactly where the oracle has it, and no NaN/Inf anywhere else."""
+    assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    excess = np.abs(o - o_ref) - (O_ATOL + O_RTOL * np.abs(o_ref))
+    if excess.max() > 0:
+        idx = np.unravel_index(np.argmax(excess), excess.shape)
+        raise AssertionError(f"{what}: O out of tolerance at {idx}: got {o[idx]} want {o_ref[idx]} "
+                             f"({int((excess > 0).sum())} of {excess.size} elements)")
+    neg = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), neg), f"{what}: -inf LSE pattern differs"
+    assert np.all(np.isfinite(lse[~neg])), f"{what}: non-finite LSE"
+    if (~neg).any():
+        err = np.abs(lse[~neg] - lse_ref[~neg]).max()
+        assert err <= LSE_ATOL, f"{what}: LSE error {err}"

@@ -1,0 +1,149 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C-ABI.
+
+Small cases are checked on every output; the full-size workloads of the pages'
+benchmarks are checked on seeded row samples (every (batch, head) pair: rows
+0, 1, 127, 128, S-1 plus random rows), launched exactly as bench.py launches them.
+"""
+import numpy as np
+import pytest
+import torch
+
+from attention_forward_07_gb300 import inputs as inp
+
+from gpu_util import assert_close, oracle_full, oracle_rows, run_cuda
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(B, Hq, Hkv, S, d, dtype, causal, mask, seed, scale=None):
+    q, k, v = inp.qkv(B, Hq, Hkv, S, d, dtype, seed)
+    if mask == "bernoulli":
+        bits = inp.pack_bits(inp.bernoulli_mask(B, S, seed))
+    elif mask == "block90":
+        bits = inp.pack_bits(inp.block_sparse_mask(B, S, seed))
+    elif mask == "sparse":
+        bits = inp.pack_bits(inp.bernoulli_mask(B, S, seed, p_keep=0.02))
+    else:
+        bits = None
+    scale = scale if scale is not None else 1.0 / d ** 0.5
+    return q, k, v, bits, causal, scale
+
+
+SMALL = [
+    # B, Hq, Hkv, S, d, dtype, causal, mask
+    (1, 2, 2, 128, 64, inp.F16, False, "bernoulli"),     # the tiny masked workload
+    (1, 1, 1, 1, 64, inp.F16, False, "none"),            # S = 1
+    (1, 1, 1, 1, 128, inp.BF16, True, "none"),
+    (2, 2, 2, 33, 128, inp.BF16, False, "none"),         # one ragged tile
+    (1, 3, 3, 129, 64, inp.BF16, True, "none"),          # 128 + 1
+    (1, 2, 2, 256, 128, inp.BF16, False, "none"),        # exactly one unit
+    (1, 2, 2, 257, 128, inp.BF16, True, "none"),         # one unit + one row
+    (2, 2, 2, 300, 128, inp.BF16, False, "none"),
+    (2, 2, 2, 300, 128, inp.BF16, True, "none"),
+    (1, 2, 2, 384, 128, inp.F16, True, "none"),          # fp16, d = 128
+    (2, 4, 2, 260, 128, inp.BF16, True, "none"),         # GQA g = 2
+    (1, 8, 1, 200, 64, inp.BF16, False, "none"),         # GQA g = 8, d = 64
+    (2, 2, 2, 300, 64, inp.F16, False, "bernoulli"),
+    (2, 2, 2, 300, 128, inp.BF16, True, "bernoulli"),    # custom AND causal
+    (2, 4, 1, 512, 64, inp.F16, False, "block90"),       # tile skipping
+    (1, 2, 2, 700, 64, inp.F16, True, "block90"),
+    (1, 2, 2, 450, 128, inp.F16, False, "sparse"),       # most rows fully masked in some tiles
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "B{}_Hq{}_Hkv{}_S{}_d{}_{}_{}_{}".format(
+    c[0], c[1], c[2], c[3], c[4], inp.DTYPE_NAME[c[5]], "causal" if c[6] else "full", c[7]))
+def test_small_full_parity(case):
+    B, Hq, Hkv, S, d, dtype, causal, mask = case
+    q, k, v, bits, causal, scale = _case(B, Hq, Hkv, S, d, dtype, causal, mask, seed=S + 17)
+    o, lse = run_cuda(q, k, v, bits, causal, scale)
+    o_ref, lse_ref = oracle_full(q, k, v, bits, causal, scale, dtype)
+    assert_close(o, lse, o_ref, lse_ref, str(case))
+
+
+def test_fully_masked_rows_and_tiles():
+    B, H, S, d = 1, 2, 300, 64
+    q, k, v = inp.qkv(B, H, H, S, d, inp.F16, 5)
+    keep = inp.bernoulli_mask(B, S, 5)
+    keep[0, 0:128] = False         # a whole query tile with nothing kept
+    keep[0, 140] = False           # single rows
+    keep[0, 299] = False
+    keep[0, :, 128:256] = False    # a whole key tile empty for every row
+    bits = inp.pack_bits(keep)
+    o, lse = run_cuda(q, k, v, bits, False, 0.125)
+    o_ref, lse_ref = oracle_full(q, k, v, bits, False, 0.125, inp.F16)
+    assert_close(o, lse, o_ref, lse_ref, "masked rows")
+    assert np.all(o[0, :, :128] == 0) and np.all(np.isneginf(lse[0, :, :128]))
+
+
+def test_causal_equals_lower_triangular_mask():
+    B, H, S, d = 2, 2, 333, 128
+    q, k, v = inp.qkv(B, H, H, S, d, inp.BF16, 9)
+    tri = inp.pack_bits(torch.tril(torch.ones((S, S), dtype=torch.bool)).expand(B, S, S))
+    a = run_cuda(q, k, v, None, True, 0.09)
+    b = run_cuda(q, k, v, tri, False, 0.09)
+    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=2e-3)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("S,causal,mask,d", [(512, False, "block90", 64), (700, True, "block90", 64),
+                                             (1000, True, "none", 128), (384, False, "bernoulli", 128),
+                                             (600, True, "sparse", 64)])
+def test_skip_map_is_exact(S, causal, mask, d):
+    B, H = 2, 3
+    q, k, v, bits, causal, scale = _case(B, H, H, S, d, inp.F16, causal, mask, seed=S)
+    o, lse, vis = run_cuda(q, k, v, bits, causal, scale, visited=True)
+    ref = oracle.skip_map(bits, B, S, causal, 128, 128)
+    assert np.array_equal(vis, np.repeat(ref[:, None], H, axis=1))
+    o_ref, lse_ref = oracle_full(q, k, v, bits, causal, scale, inp.F16)
+    assert_close(o, lse, o_ref, lse_ref, "visited run")
+
+
+def test_deterministic():
+    q, k, v, bits, causal, scale = _case(2, 4, 2, 777, 128, inp.BF16, True, "none", seed=3)
+    a = run_cuda(q, k, v, bits, causal, scale)
+    b = run_cuda(q, k, v, bits, causal, scale)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1], equal_nan=True)
+
+
+def test_many_units_per_cta_sampled():
+    """More work units than SMs: every CTA walks several units of the persistent loop."""
+    B, Hq, Hkv, S, d = 4, 8, 2, 2304, 128
+    for causal in (False, True):
+        q, k, v, bits, causal, scale = _case(B, Hq, Hkv, S, d, inp.BF16, causal, "none", seed=11)
+        o, lse = run_cuda(q, k, v, bits, causal, scale)
+        rows = inp.sample_rows(B, Hq, S, 24, seed=1)
+        o_ref, lse_ref = oracle_rows(q, k, v, bits, causal, scale, inp.BF16, rows)
+        assert_close(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, f"causal={causal}")
+
+
+# ------------------------------------------------------------------------ full-size workloads
+
+SHORT = ["tiny_masked", "short_masked", "short_masked90"]
+PREFILL = [n for n in inp.WORKLOADS if n not in SHORT]
+
+
+@pytest.mark.parametrize("name", SHORT)
+def test_short_workloads_full_parity(name):
+    w = inp.WORKLOADS[name]
+    q, k, v, bits = w.make(w.seed(list(inp.WORKLOADS).index(name)))
+    o, lse, vis = run_cuda(q, k, v, bits, w.causal, w.scale, visited=True)
+    o_ref, lse_ref = oracle_full(q, k, v, bits, w.causal, w.scale, w.dtype)
+    assert_close(o, lse, o_ref, lse_ref, name)
+    ref = oracle.skip_map(bits, w.B, w.S, w.causal, 128, 128)
+    assert np.array_equal(vis, np.repeat(ref[:, None], w.Hq, axis=1))
+
+
+@pytest.mark.parametrize("name", PREFILL)
+def test_prefill_workloads_sampled_parity(name):
+    w = inp.WORKLOADS[name]
+    q, k, v, bits = w.make(w.seed(list(inp.WORKLOADS).index(name)))
+    o, lse = run_cuda(q, k, v, bits, w.causal, w.scale)
+    rows = inp.sample_rows(w.B, w.Hq, w.S, 4, seed=w.S)
+    o_ref, lse_ref = oracle_rows(q, k, v, bits, w.causal, w.scale, w.dtype, rows)
+    assert_close(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, name)
+    # properties that hold at any size, checked on every row: finite outputs, |O| <= max|V|
+    vmax = float(v.float().abs().max())
+    assert np.all(np.isfinite(lse)) and np.abs(o).max() <= vmax * (1 + 1e-2)
