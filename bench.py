@@ -1,0 +1,404 @@
+"""Benchmark: fused attention forward on GB300, one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one launch of the fused forward over one batch of the workload (inputs
+resident in HBM).  Default workload: causal GQA prefill, Hq=32, Hkv=8, d=128, bf16,
+S=8192, B=4 (B*S = 32768 tokens) -- the prefill configuration that runs the most of
+the path at once (scheduler with longest-first causal order, causal bit masking and
+tile skipping, GQA head mapping, both tensor-core contractions, online softmax,
+correction, epilogue).  Every other workload of the pages is available through
+--workload.
+
+Under torchrun (--gpus N > 1) every rank runs its own replica of the workload on its
+own GPU (weak scaling, no collective on the data path); the timed region is bracketed
+by barriers and the slowest rank's time is reported.
+
+--impl reference times the fp64 CPU oracle (the only reference implementation this
+project has) on a bounded random row sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (GB300, 1 GPU) and % of dense BF16 peak / roofline"
+DEFAULT_WORKLOAD = "gqa8_causal_S8192"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each rank's replica draws its own inputs (weak scaling: the per-GPU work is fixed)."""
+    return base_seed + 7919 * rank
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- workload helpers
+
+def workload(name: str, batch: int = 0):
+    from dataclasses import replace
+    from attention_forward_07_gb300 import inputs as inp
+    if name not in inp.WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(inp.WORKLOADS)}")
+    w = inp.WORKLOADS[name]
+    if batch:
+        w = replace(w, B=batch)
+    return w, list(inp.WORKLOADS).index(name)
+
+
+def algorithmic_bytes(w) -> int:
+    """Compulsory HBM traffic of one launch: Q, K, V read once, O and LSE written once,
+    mask words read once."""
+    el = 2
+    q = w.B * w.Hq * w.S * w.d * el
+    kv = 2 * w.B * w.Hkv * w.S * w.d * el
+    o = q
+    lse = w.B * w.Hq * w.S * 4
+    mask = w.B * w.S * ((w.S + 31) // 32) * 4 if w.mask != "none" else 0
+    return q + kv + o + lse + mask
+
+
+def config_dict(w, name, n):
+    return {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
+            "causal": w.causal, "mask": w.mask,
+            "dtype_in": {0: "f16", 1: "bf16"}[w.dtype], "global_batch": w.B * n, "seq_len": w.S,
+            "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
+            "l2": ("inputs larger than L2, no flush" if algorithmic_bytes(w) > 2 * L2_BYTES
+                   else "L2 flushed (256 MiB write) between timed launches")}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool = True):
+        self.proc = None
+        self.lines = []
+        self.index = index
+        if enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
+        self.t_start = self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for nm, val in zip(names, r[5:9]):
+                if val.strip() == "Active":
+                    reasons.add(nm)
+        # keep the samples taken under load (clock above idle) if any
+        load = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- the oracle baseline
+
+def cpu_baseline(w, seed, target_seconds: float):
+    """The fp64 oracle, as it stands, on a bounded random row sample of the workload.
+    Returns (TFLOPS-equivalent, threads, sample description, seconds)."""
+    import oracle
+    from attention_forward_07_gb300 import inputs as inp
+    q, k, v, bits = w.make(seed)
+    total_rows = w.B * w.Hq * w.S
+    rng = np.random.default_rng(seed)
+    # calibrate on a small sample, then size the timed sample to ~target_seconds
+    probe = rng.choice(total_rows, size=min(total_rows, 256), replace=False).astype(np.int64)
+    args = (inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), w.dtype)
+    t0 = time.perf_counter()
+    oracle.attn_rows(*args, probe, bits, w.causal, w.scale)
+    rate = len(probe) / max(time.perf_counter() - t0, 1e-6)
+    n = int(min(total_rows, max(256, rate * target_seconds)))
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attn_rows(*args, rows, bits, w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    flops = w.flops() * n / total_rows
+    return flops / dt / 1e12, oracle.num_threads(), f"{n} random rows of {total_rows} (seeded), fp64", dt
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w, idx = workload(args.workload, args.batch)
+    import oracle
+    from attention_forward_07_gb300 import inputs as inp
+    oracle.build()
+    seed = w.seed(idx)
+    q, k, v, bits = w.make(seed)
+    a = (inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), w.dtype)
+    total_rows = w.B * w.Hq * w.S
+    rng = np.random.default_rng(seed)
+    per_step = int(min(total_rows, 2048))
+    times = []
+    for step in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(total_rows, size=per_step, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attn_rows(*a, rows, bits, w.causal, w.scale)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    dt = sum(times)
+    flops = w.flops() * per_step / total_rows * len(times)
+    value = flops / dt / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(1, len(times)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": config_dict(w, args.workload, 1),
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{per_step} random rows of {total_rows} per step (seeded), fp64"},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+# DRAM bytes (read + write) per launch from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`,
+# keyed by the sha1 of the kernel sources they were taken on; a changed kernel reports null.
+MEASURED_TRAFFIC = {}
+
+
+def kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "attention_forward_07_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+def roofline(w, seconds_per_launch):
+    p_tensor, p_hbm, src = peaks()
+    flops, nbytes = w.flops(), algorithmic_bytes(w)
+    t_tensor = flops / (p_tensor * 1e12)
+    t_hbm = nbytes / (p_hbm * 1e9)
+    traffic = MEASURED_TRAFFIC.get(kernel_hash(), {}).get(config_key(w))
+    if t_tensor >= t_hbm:
+        ach = flops / seconds_per_launch / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": p_tensor, "unit": "TFLOP/s", "frac": ach / p_tensor,
+                "traffic": traffic, "peak_source": f"{src} bf16 dense (burst)",
+                "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
+    ach = nbytes / seconds_per_launch / 1e9
+    return {"bound": "hbm", "achieved": ach, "peak": p_hbm, "unit": "GB/s", "frac": ach / p_hbm,
+            "traffic": traffic, "peak_source": f"{src} HBM copy", "algorithmic_flops": flops,
+            "algorithmic_bytes": nbytes}
+
+
+def config_key(w):
+    return f"B{w.B}_Hq{w.Hq}_Hkv{w.Hkv}_S{w.S}_d{w.d}_{'causal' if w.causal else 'full'}_{w.mask}"
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if args.gpus != world:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N>1 through torchrun")
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import attention_forward_07_gb300 as af
+    af.library()  # fail loudly here if the CUDA library is missing
+    w, idx = workload(args.workload, args.batch)
+    seed = replica_seed(w.seed(idx), rank)
+    q, k, v, bits = w.make(seed)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if bits is None else torch.from_numpy(bits.view(np.int32)).to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    flush = algorithmic_bytes(w) <= 2 * L2_BYTES
+    fbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+
+    def step():
+        af.attn_fwd(qd, kd, vd, o, lse, md, causal=w.causal, scale=w.scale)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    af.attn_check()
+
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    time.sleep(0.4 if sampler.proc else 0)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.mark_start()
+    for i in range(K):
+        if flush:
+            fbuf.fill_(i & 0xFF)
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    sampler.mark_end()
+    af.attn_check()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    t_ms = sum(per_launch_ms)
+    t_ms = max_over_ranks(t_ms, world, dev)
+    clocks = sampler.stop() if sampler.proc else None
+    value = world * w.flops() * K / (t_ms / 1e3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, max(3, min(K, 20)), world)
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": t_ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": {0: "f16", 1: "bf16"}[w.dtype], "data": "synthetic",
+            "config": config_dict(w, args.workload, world),
+            "roofline": roofline(w, statistics.mean(per_launch_ms) / 1e3),
+            "gpu_launches": K, "clocks": clocks, "e2e": e2e, "kernel": kernel_hash()}
+    line["roofline"]["launch_ms_median"] = statistics.median(per_launch_ms)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, cores, sample, secs = cpu_baseline(w, seed, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample,
+                                "seconds": secs}
+    else:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world):
+    """Same metric through the public API with host buffers: every step copies Q, K, V
+    (and the mask) from pinned host memory, runs the forward, and reads O and LSE back."""
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    mh = None if bits is None else torch.from_numpy(bits.view(np.int32)).pin_memory()
+    qd, kd, vd = torch.empty_like(qh, device=dev), torch.empty_like(kh, device=dev), torch.empty_like(vh, device=dev)
+    md = None if mh is None else torch.empty_like(mh, device=dev)
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        if md is not None:
+            md.copy_(mh, non_blocking=True)
+        af.attn_fwd(qd, kd, vd, o, lse, md, causal=w.causal, scale=w.scale)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize(dev)
+    af.attn_check()
+    ms = max_over_ranks(s.elapsed_time(e), world, dev) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (0 if mh is None else mh.numel() * 4)
+    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+    return {"value": world * w.flops() / (ms / 1e3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
