@@ -50,6 +50,8 @@ constexpr int QT = 2;          // Q tiles per work unit
 constexpr int UNIT_ROWS = BM * QT;
 constexpr int BN = 128;        // keys per K/V tile
 constexpr int NTHREADS = 384;  // 12 warps
+constexpr int REGS_LAUNCH = 168, REGS_LOADMMA = 80, REGS_SOFTMAX = 208;
+static_assert(128 * REGS_LOADMMA + 256 * REGS_SOFTMAX <= NTHREADS * REGS_LAUNCH, "register split");
 constexpr int NINFO = 4;       // depth of the tile-descriptor ring
 constexpr int TMEM_COLS = 512;
 constexpr int S_COL0 = 0;      // S_t (fp32, 128 columns) at t*128; P_t aliases its first 64
@@ -65,16 +67,26 @@ struct Layout {
   static constexpr int HALVES = D / 64;                  // 128-byte swizzle spans per row
   static constexpr int Q_TILE_BYTES = BM * D * 2;
   static constexpr int KV_TILE_BYTES = BN * D * 2;
-  static constexpr int NSLOT = (D == 128) ? (MODE == MASK_CUSTOM ? 4 : 5) : 8;
+  // d = 64 (short sequences, many units per CTA) double-buffers the Q tiles so the next
+  // unit's Q load overlaps the current unit; d = 128 spends that room on K/V slots.
+  static constexpr int QBUF = (D == 64) ? 2 : 1;
+  // Separate K and V rings: K(j) is read by the two QK^T of tile j, V(j) by the two P.V
+  // one tile later, so each ring is released right after its own last reader.
+  static constexpr int KSLOT = (D == 128) ? (MODE == MASK_CUSTOM ? 2 : 3) : 4;
+  static constexpr int VSLOT = (D == 128) ? 2 : 4;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + QT * Q_TILE_BYTES;
-  static constexpr int OFF_WORDS = OFF_KV + NSLOT * KV_TILE_BYTES;
+  static constexpr int Q_BUF_BYTES = QT * Q_TILE_BYTES;
+  static constexpr int OFF_K = OFF_Q + QBUF * Q_BUF_BYTES;
+  static constexpr int OFF_V = OFF_K + KSLOT * KV_TILE_BYTES;
+  static constexpr int OFF_WORDS = OFF_V + VSLOT * KV_TILE_BYTES;
   static constexpr int WORDS_PER_ENTRY = UNIT_ROWS * (BN / 32);
   static constexpr int OFF_HDR = OFF_WORDS + (MODE == MASK_CUSTOM ? NINFO * WORDS_PER_ENTRY * 4 : 0);
   static constexpr int OFF_BAR = OFF_HDR + NINFO * 16;
   // barrier indices
-  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_SFULL = 2, B_SEMPTY = 2 + NSLOT,
-                       B_IFULL = 2 + 2 * NSLOT, B_IEMPTY = B_IFULL + NINFO,
+  static constexpr int B_QFULL = 0, B_QEMPTY = QBUF, B_KFULL = 2 * QBUF,
+                       B_KEMPTY = B_KFULL + KSLOT, B_VFULL = B_KEMPTY + KSLOT,
+                       B_VEMPTY = B_VFULL + VSLOT, B_IFULL = B_VEMPTY + VSLOT,
+                       B_IEMPTY = B_IFULL + NINFO,
                        B_STILE = B_IEMPTY + NINFO, B_PREADY = B_STILE + QT,
                        B_ODONE = B_PREADY + QT, B_DRAIN = B_ODONE + QT, NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -112,9 +124,10 @@ __device__ unsigned int g_attn_status;
 
 namespace attn {
 
-// Slow path of a bounded barrier wait.  Gives up when another thread has aborted, when
+// Slow path of a bounded barrier wait (inlined: a shared non-inlined callee cannot serve
+// warps running under different setmaxnreg budgets).  Gives up when another thread has aborted, when
 // the wait has lasted timeout_ns, or after an iteration cap, and then aborts the CTA.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        unsigned long long timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
@@ -141,7 +154,7 @@ __device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity, volati
 }
 
 // Wait used only while draining after an abort: ignores the abort flag, short limit.
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; it < (1u << 24); ++it) {
     if (mbar_try_wait(bar, parity)) return;
@@ -208,11 +221,13 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
   uint32_t* words = reinterpret_cast<uint32_t*>(gbase + L::OFF_WORDS);
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
 
-  uint32_t q_empty_par = 1;     // producer waits on "empty" barriers starting from parity 1
-  uint32_t q_fills = 0;         // Q loads issued so far
-  int slot = 0;
-  uint32_t slot_par = 1;
-  uint32_t pend_mask = 0, pend_par = 0;  // slots with a load issued, and its full-barrier parity
+  uint32_t q_empty_par = (1u << L::QBUF) - 1u;  // per Q buffer; "empty" waits start at parity 1
+  uint32_t q_pend = 0, q_pend_par = 0;           // Q buffers with a load issued, its full parity
+  // ring position and "empty" parity of the K and V rings; loads issued but possibly not
+  // landed (bit per slot) and the full-barrier parity each of those loads completes
+  int kslot = 0, vslot = 0;
+  uint32_t kpar = 1, vpar = 1;
+  uint32_t kpend = 0, kpend_par = 0, vpend = 0, vpend_par = 0;
   int ie = 0;
   uint32_t ie_par = 1;
   bool inject = p.inject != 0;
@@ -226,20 +241,24 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     const int row0 = qb * UNIT_ROWS;
 
     // Both Q tiles of the unit (rows past S are zero-filled by the TMA unit).
-    if (!bwait_warp(bars + 8u * L::B_QEMPTY, q_empty_par, abort_flag, to)) goto drain;
-    q_empty_par ^= 1u;
+    const int qbuf = k % L::QBUF;
+    if (!bwait_warp(bars + 8u * (L::B_QEMPTY + qbuf), (q_empty_par >> qbuf) & 1u, abort_flag, to))
+      goto drain;
+    q_empty_par ^= 1u << qbuf;
     if (!inject) {
       if (lane == 0) {
-        const uint32_t fb = bars + 8u * L::B_QFULL;
-        mbar_expect_tx(fb, QT * L::Q_TILE_BYTES);
+        const uint32_t fb = bars + 8u * (L::B_QFULL + qbuf);
+        mbar_expect_tx(fb, L::Q_BUF_BYTES);
 #pragma unroll
         for (int t = 0; t < QT; ++t)
 #pragma unroll
           for (int h = 0; h < L::HALVES; ++h)
-            tma_load_3d(base + L::OFF_Q + t * L::Q_TILE_BYTES + h * BM * 128, &p.tm_q, fb, h * 64,
-                        row0 + t * BM, b * p.Hq + hq);
+            tma_load_3d(base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES + h * BM * 128,
+                        &p.tm_q, fb, h * 64, row0 + t * BM, b * p.Hq + hq);
       }
-      ++q_fills;
+      // this fill completes the phase the consumer waits for with parity (empty parity ^ 1)
+      q_pend |= 1u << qbuf;
+      q_pend_par = (q_pend_par & ~(1u << qbuf)) | ((((q_empty_par >> qbuf) & 1u)) << qbuf);
     }
     inject = false;
 
@@ -296,21 +315,32 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       mbar_arrive(bars + 8u * (L::B_IFULL + ie));
       if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
 
-      for (int kv = 0; kv < 2; ++kv) {  // K tile, then V tile
-        if (!bwait_warp(bars + 8u * (L::B_SEMPTY + slot), slot_par, abort_flag, to)) goto drain;
-        if (lane == 0) {
-          const uint32_t fb = bars + 8u * (L::B_SFULL + slot);
-          mbar_expect_tx(fb, L::KV_TILE_BYTES);
+      // K tile j
+      if (!bwait_warp(bars + 8u * (L::B_KEMPTY + kslot), kpar, abort_flag, to)) goto drain;
+      if (lane == 0) {
+        const uint32_t fb = bars + 8u * (L::B_KFULL + kslot);
+        mbar_expect_tx(fb, L::KV_TILE_BYTES);
 #pragma unroll
-          for (int h = 0; h < L::HALVES; ++h)
-            tma_load_3d(base + L::OFF_KV + slot * L::KV_TILE_BYTES + h * BN * 128,
-                        kv ? (const void*)&p.tm_v : (const void*)&p.tm_k, fb, h * 64, j * BN,
-                        b * p.Hkv + hkv);
-        }
-        pend_mask |= 1u << slot;
-        pend_par = (pend_par & ~(1u << slot)) | ((slot_par ^ 1u) << slot);
-        if (++slot == L::NSLOT) { slot = 0; slot_par ^= 1u; }
+        for (int h = 0; h < L::HALVES; ++h)
+          tma_load_3d(base + L::OFF_K + kslot * L::KV_TILE_BYTES + h * BN * 128, &p.tm_k, fb,
+                      h * 64, j * BN, b * p.Hkv + hkv);
       }
+      kpend |= 1u << kslot;
+      kpend_par = (kpend_par & ~(1u << kslot)) | ((kpar ^ 1u) << kslot);
+      if (++kslot == L::KSLOT) { kslot = 0; kpar ^= 1u; }
+      // V tile j
+      if (!bwait_warp(bars + 8u * (L::B_VEMPTY + vslot), vpar, abort_flag, to)) goto drain;
+      if (lane == 0) {
+        const uint32_t fb = bars + 8u * (L::B_VFULL + vslot);
+        mbar_expect_tx(fb, L::KV_TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < L::HALVES; ++h)
+          tma_load_3d(base + L::OFF_V + vslot * L::KV_TILE_BYTES + h * BN * 128, &p.tm_v, fb,
+                      h * 64, j * BN, b * p.Hkv + hkv);
+      }
+      vpend |= 1u << vslot;
+      vpend_par = (vpend_par & ~(1u << vslot)) | ((vpar ^ 1u) << vslot);
+      if (++vslot == L::VSLOT) { vslot = 0; vpar ^= 1u; }
     }
     // End-of-unit marker.
     if (!bwait_warp(bars + 8u * (L::B_IEMPTY + ie), ie_par, abort_flag, to)) goto drain;
@@ -327,9 +357,12 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
 drain:
   // Aborted: let the copies this warp started land before the CTA exits.
   if (lane == 0) {
-    for (int s = 0; s < L::NSLOT; ++s)
-      if ((pend_mask >> s) & 1u) wait_drain(bars + 8u * (L::B_SFULL + s), (pend_par >> s) & 1u);
-    if (q_fills > 0) wait_drain(bars + 8u * L::B_QFULL, (q_fills - 1u) & 1u);
+    for (int s = 0; s < L::KSLOT; ++s)
+      if ((kpend >> s) & 1u) wait_drain(bars + 8u * (L::B_KFULL + s), (kpend_par >> s) & 1u);
+    for (int s = 0; s < L::VSLOT; ++s)
+      if ((vpend >> s) & 1u) wait_drain(bars + 8u * (L::B_VFULL + s), (vpend_par >> s) & 1u);
+    for (int qb2 = 0; qb2 < L::QBUF; ++qb2)
+      if ((q_pend >> qb2) & 1u) wait_drain(bars + 8u * (L::B_QFULL + qb2), (q_pend_par >> qb2) & 1u);
   }
   __syncwarp();
 }
@@ -338,14 +371,17 @@ drain:
 
 namespace attn {
 
-// ------------------------------------------------------------------ MMA issuer (warp 1, lane 0)
-// Per tile descriptor e (key tile j) and Q tile t, in this order:
+// ------------------------------------------------------------------ MMA issuer (warp 1)
+// The whole warp runs this code converged (descriptors in uniform registers); elect.sync
+// picks the lane that issues each tcgen05 instruction.  Per tile descriptor e (key tile j)
+// and Q tile t, in this order:
 //   O_t (+)= P_t(prev) . V(prev)    once softmax t has written P for the previous tile
 //   S_t     = Q_t . K(j)^T          then signal softmax t
-// so S_t / P_t (which share TMEM columns) are rewritten only after the P.V that reads them.
+// so S_t / P_t (which share TMEM columns) are rewritten only after the P.V that reads
+// them.  Each ring slot is released by a commit right after its last reader.
 template <int D, bool BF16, int MODE>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t* gbase,
-                                         volatile int* abort_flag, uint32_t tmem) {
+                                         volatile int* abort_flag, uint32_t tmem, int lane) {
   using L = Layout<D, MODE>;
   const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
   const unsigned long long to = p.timeout_ns;
@@ -354,96 +390,101 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
   constexpr uint32_t ID_QK = idesc_f16acc32(BF16, false, false, BM, BN);
   constexpr uint32_t ID_PV = idesc_f16acc32(BF16, false, true, BM, D);
 
-  uint32_t q_par = 0, ie_par = 0, slot_par = 0, p_par0 = 0, p_par1 = 0;
-  int slot = 0, ie = 0;
+  uint32_t q_par = 0, ie_par = 0, kpar = 0, vpar = 0, p_par0 = 0, p_par1 = 0;  // q_par: bit per Q buffer
+  int kslot = 0, vslot = 0, ie = 0;
 
   for (int k = 0;; ++k) {
     const int u = unit_at(k, p.num_units);
     if (u < 0) break;
     int b, hq, qb;
     decode_unit(u, p, causal, b, hq, qb);
-    if (!bwait(bars + 8u * L::B_QFULL, q_par, abort_flag, to)) goto drain;
-    q_par ^= 1u;
+    const int qbuf = k % L::QBUF;
+    if (!bwait_warp(bars + 8u * (L::B_QFULL + qbuf), (q_par >> qbuf) & 1u, abort_flag, to)) goto drain;
+    q_par ^= 1u << qbuf;
     tc_fence_after();
 
     bool have_prev = false, pv0 = false, pv1 = false;
     int prev_flags = 0, prev_vslot = 0;
     uint32_t prev_vpar = 0;
     while (true) {
-      if (!bwait(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) goto drain;
+      if (!bwait_warp(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) goto drain;
       const int j = hdr[ie].j;
       const int flags = hdr[ie].flags;
       const bool end = (flags & FLAG_END) != 0;
-      int kslot = 0, vslot = 0;
-      uint32_t vpar = 0;
+      const int cur_kslot = kslot, cur_vslot = vslot;
+      const uint32_t cur_kpar = kpar, cur_vpar = vpar;
       if (!end) {
-        kslot = slot;
-        const uint32_t kpar = slot_par;
-        if (++slot == L::NSLOT) { slot = 0; slot_par ^= 1u; }
-        vslot = slot;
-        vpar = slot_par;
-        if (++slot == L::NSLOT) { slot = 0; slot_par ^= 1u; }
-        if (!bwait(bars + 8u * (L::B_SFULL + kslot), kpar, abort_flag, to)) goto drain;
+        if (++kslot == L::KSLOT) { kslot = 0; kpar ^= 1u; }
+        if (++vslot == L::VSLOT) { vslot = 0; vpar ^= 1u; }
       }
-      if (have_prev && !bwait(bars + 8u * (L::B_SFULL + prev_vslot), prev_vpar, abort_flag, to))
-        goto drain;
-      tc_fence_after();
+      if (have_prev) {
+        if (!bwait_warp(bars + 8u * (L::B_VFULL + prev_vslot), prev_vpar, abort_flag, to)) goto drain;
+        tc_fence_after();
+      }
+      bool k_ready = false;
 
 #pragma unroll
       for (int t = 0; t < QT; ++t) {
         const uint32_t s_col = tmem + S_COL0 + t * 128;
         if (have_prev && ((prev_flags >> t) & 1)) {
           uint32_t& pp = t ? p_par1 : p_par0;
-          if (!bwait(bars + 8u * (L::B_PREADY + t), pp, abort_flag, to)) goto drain;
+          if (!bwait_warp(bars + 8u * (L::B_PREADY + t), pp, abort_flag, to)) goto drain;
           pp ^= 1u;
           tc_fence_after();
           bool& started = t ? pv1 : pv0;
-          const uint32_t vbase = base + L::OFF_KV + prev_vslot * L::KV_TILE_BYTES;
+          const uint32_t vbase = base + L::OFF_V + prev_vslot * L::KV_TILE_BYTES;
           // V tile as the MN-major B operand: 16 keys per step (2048 bytes), the two
           // 64-column halves of d are KV_TILE_BYTES/2 apart, 8-key groups 1024 apart.
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + O_COL0 + t * 128, s_col + kk * 8,
-                   sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
-                   (started || kk > 0) ? 1u : 0u);
+            mma_ts_elect(tmem + O_COL0 + t * 128, s_col + kk * 8,
+                         sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
+                         (started || kk > 0) ? 1u : 0u);
           started = true;
         }
+        if (t == QT - 1 && have_prev) tc_commit_elect(bars + 8u * (L::B_VEMPTY + prev_vslot));
         if (!end && ((flags >> t) & 1)) {
-          const uint32_t qbase = base + L::OFF_Q + t * L::Q_TILE_BYTES;
-          const uint32_t kbase = base + L::OFF_KV + kslot * L::KV_TILE_BYTES;
+          if (!k_ready) {
+            if (!bwait_warp(bars + 8u * (L::B_KFULL + cur_kslot), cur_kpar, abort_flag, to)) goto drain;
+            tc_fence_after();
+            k_ready = true;
+          }
+          const uint32_t qbase = base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES;
+          const uint32_t kbase = base + L::OFF_K + cur_kslot * L::KV_TILE_BYTES;
           // Q and K as K-major operands: 16 elements (32 bytes) per step inside a
           // 128-byte swizzle row, the next 64 elements one half-tile further.
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            mma_ss(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                   ID_QK, kk > 0 ? 1u : 0u);
+            mma_ss_elect(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                         ID_QK, kk > 0 ? 1u : 0u);
           }
-          tc_commit(bars + 8u * (L::B_STILE + t));
-          if (p.visited)
+          tc_commit_elect(bars + 8u * (L::B_STILE + t));
+          if (p.visited && lane == 0)
             p.visited[((size_t)(b * p.Hq + hq) * p.nqt + (qb * QT + t)) * p.nkt + j] = 1;
+          __syncwarp();
         }
       }
-      if (have_prev) tc_commit(bars + 8u * (L::B_SEMPTY + prev_vslot));
-      if (!end) tc_commit(bars + 8u * (L::B_SEMPTY + kslot));
-      mbar_arrive(bars + 8u * (L::B_IEMPTY + ie));
+      if (!end) tc_commit_elect(bars + 8u * (L::B_KEMPTY + cur_kslot));
+      mbar_arrive_elect(bars + 8u * (L::B_IEMPTY + ie));
       if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
       if (end) break;
       have_prev = true;
       prev_flags = flags;
-      prev_vslot = vslot;
-      prev_vpar = vpar;
+      prev_vslot = cur_vslot;
+      prev_vpar = cur_vpar;
     }
-    if (pv0) tc_commit(bars + 8u * (L::B_ODONE + 0));
-    if (pv1) tc_commit(bars + 8u * (L::B_ODONE + 1));
-    tc_commit(bars + 8u * L::B_QEMPTY);
+    if (pv0) tc_commit_elect(bars + 8u * (L::B_ODONE + 0));
+    if (pv1) tc_commit_elect(bars + 8u * (L::B_ODONE + 1));
+    tc_commit_elect(bars + 8u * (L::B_QEMPTY + qbuf));
   }
   return;
 
 drain:
-  // Aborted: wait until every MMA this thread issued has finished before TMEM is freed.
-  tc_commit(bars + 8u * L::B_DRAIN);
+  // Aborted: wait until every MMA this warp issued has finished before TMEM is freed.
+  tc_commit_elect(bars + 8u * L::B_DRAIN);
   wait_drain(bars + 8u * L::B_DRAIN, 0);
+  __syncwarp();
 }
 
 }  // namespace attn
@@ -501,55 +542,103 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       if (!bwait_warp(bars + 8u * (L::B_STILE + t), s_par, abort_flag, to)) return;
       s_par ^= 1u;
       tc_fence_after();
+      // Scores: the first 64 columns are loaded and reduced while the last 64 are in flight.
       uint32_t sr[128];
-      tmem_ld32x32b_x128_wait(s_addr, sr);
+      uint32_t(&sa)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[0]);
+      uint32_t(&sb)[64] = *reinterpret_cast<uint32_t(*)[64]>(&sr[64]);
+      tmem_ld32x32b_x64_wait(s_addr, sa);
+      tmem_ld32x32b_x64(s_addr + 64, sb);
 
       // Mask: excluded scores become -inf (weight exactly 0).
-      if constexpr (MODE == MASK_CUSTOM) {
-        const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      int lim = p.S - j * BN;  // keys at or past S
+      if (MODE == MASK_CAUSAL) lim = min(lim, i - j * BN + 1);
+      const bool edge = (MODE != MASK_CUSTOM) && __any_sync(0xffffffffu, lim < BN);
+      const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      auto mask_half = [&](uint32_t(&h)[64], int c0) {
+        if constexpr (MODE == MASK_CUSTOM) {
 #pragma unroll
-        for (int cc = 0; cc < 128; ++cc)
-          if (!((wa[cc >> 5] >> (cc & 31)) & 1u)) sr[cc] = __float_as_uint(-INFINITY);
-      } else {
-        int lim = p.S - j * BN;  // keys at or past S
-        if (MODE == MASK_CAUSAL) lim = min(lim, i - j * BN + 1);
-        if (__any_sync(0xffffffffu, lim < BN)) {
+          for (int cc = 0; cc < 64; ++cc)
+            if (!((wa[(c0 + cc) >> 5] >> ((c0 + cc) & 31)) & 1u)) h[cc] = __float_as_uint(-INFINITY);
+        } else if (edge) {
 #pragma unroll
-          for (int cc = 0; cc < 128; ++cc)
-            if (cc >= lim) sr[cc] = __float_as_uint(-INFINITY);
+          for (int cc = 0; cc < 64; ++cc)
+            if (c0 + cc >= lim) h[cc] = __float_as_uint(-INFINITY);
         }
-      }
-
-      float mx = -INFINITY;
+      };
+      // Row max of one half: four independent 3-input max chains, chain x over h[16x, 16x+16).
+      auto max_half = [&](const uint32_t(&h)[64]) {
+        float a4[4];
 #pragma unroll
-      for (int cc = 0; cc < 128; ++cc) mx = fmaxf(mx, __uint_as_float(sr[cc]));
-      const float m_new = fmaxf(m, mx * c);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+        for (int x = 0; x < 4; ++x) {
+          a4[x] = fmaxf(__uint_as_float(h[16 * x]), __uint_as_float(h[16 * x + 1]));
+#pragma unroll
+          for (int e = 2; e < 16; e += 2)
+            a4[x] = fmax3(a4[x], __uint_as_float(h[16 * x + e]), __uint_as_float(h[16 * x + e + 1]));
+        }
+        return fmax3(a4[0], a4[1], fmaxf(a4[2], a4[3]));
+      };
+      mask_half(sa, 0);
+      const float mx_a = max_half(sa);
+      tmem_wait_ld();
+      tmem_fence_regs_x64(sb);
+      mask_half(sb, 64);
+      const float mx = fmaxf(mx_a, max_half(sb));
 
-      // Correction: rescale this row of O when its running max grew.
-      if (nact > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // Lazy rescaling: the exponent base m only moves when the row max exceeds it by more
+      // than 8 (weights stay <= 2^8); O and l are always scaled with the same base, so the
+      // final O / l and LSE = ln2 * (m + log2 l) are exact.
+      const float mx_s = mx * c;
+      const bool grow = mx_s > m + 8.f;  // also true on the first kept key (m = -inf)
+      const float m_new = grow ? mx_s : m;
+      const float alpha = grow ? ex2_approx(m - m_new) : 1.f;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+
+      // Correction: rescale this row of O (only warps where some row moved its base).
+      if (nact > 0 && __any_sync(0xffffffffu, grow)) {
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t ob[32];
           tmem_ld32x32b_x32_wait(o_addr + ch * 32, ob);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) ob[x] = __float_as_uint(__uint_as_float(ob[x]) * alpha);
+          for (int x = 0; x < 16; ++x) {
+            float lo, hi;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(ob[2 * x]), __uint_as_float(ob[2 * x + 1])), a2), lo, hi);
+            ob[2 * x] = __float_as_uint(lo);
+            ob[2 * x + 1] = __float_as_uint(hi);
+          }
           tmem_st32x32b_x32(o_addr + ch * 32, ob);
         }
       }
 
-      float sum = 0.f;
-      uint32_t pk[64];
+      // P = 2^(s*c - m): packed FMA for the arguments, MUFU ex2, four packed partial sums.
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      // P_t goes over the first 64 columns of S_t, in two stores so the first overlaps
+      // the exponentials of the second half.
 #pragma unroll
-      for (int cc = 0; cc < 64; ++cc) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc]), c, -m_use));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc + 1]), c, -m_use));
-        sum += p0 + p1;
-        pk[cc] = pack2<BF16>(p0, p1);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) {
+          const int e = hh * 32 + cc;
+          float e0, e1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2, nm2), e0, e1);
+          const float p0 = ex2_approx(e0);
+          const float p1 = ex2_approx(e1);
+          acc[cc & 3] = fadd2(acc[cc & 3], f2_pack(p0, p1));
+          pk[cc] = pack2<BF16>(p0, p1);
+        }
+        tmem_st32x32b_x32(s_addr + hh * 32, pk);
       }
-      tmem_st32x32b_x64(s_addr, pk);  // P_t over the first 64 columns of S_t
       tmem_wait_st();
+      float s0, s1, s2, s3, s4, s5, s6, s7;
+      f2_unpack(acc[0], s0, s1);
+      f2_unpack(acc[1], s2, s3);
+      f2_unpack(acc[2], s4, s5);
+      f2_unpack(acc[3], s6, s7);
+      const float sum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
       l = l * alpha + sum;
       m = m_new;
       tc_fence_before();
@@ -604,11 +693,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t bars = base + L::OFF_BAR;
 
   if (threadIdx.x == 0) {
-    mbar_init(bars + 8u * L::B_QFULL, 1);
-    mbar_init(bars + 8u * L::B_QEMPTY, 1);
-    for (int s = 0; s < L::NSLOT; ++s) {
-      mbar_init(bars + 8u * (L::B_SFULL + s), 1);
-      mbar_init(bars + 8u * (L::B_SEMPTY + s), 1);
+    for (int qb2 = 0; qb2 < L::QBUF; ++qb2) {
+      mbar_init(bars + 8u * (L::B_QFULL + qb2), 1);
+      mbar_init(bars + 8u * (L::B_QEMPTY + qb2), 1);
+    }
+    for (int s = 0; s < L::KSLOT; ++s) {
+      mbar_init(bars + 8u * (L::B_KFULL + s), 1);
+      mbar_init(bars + 8u * (L::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < L::VSLOT; ++s) {
+      mbar_init(bars + 8u * (L::B_VFULL + s), 1);
+      mbar_init(bars + 8u * (L::B_VEMPTY + s), 1);
     }
     for (int e = 0; e < NINFO; ++e) {
       mbar_init(bars + 8u * (L::B_IFULL + e), 32);                // the whole load warp
@@ -637,12 +732,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    load_role<D, BF16, MODE>(p, base, gbase, abort_flag, lane);
-  } else if (warp == 1) {
-    if (lane == 0) mma_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem);
-    __syncwarp();
-  } else if (warp >= 4) {
+  // Register rebalancing: the load / MMA warpgroup (warps 0-3) needs few registers, the
+  // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 80 + 256 x 208 + 1024.
+  // Each setmaxnreg sits in the same branch as the code it budgets for.
+  if (warp < 4) {
+    setmaxnreg_dec<REGS_LOADMMA>();
+    if (warp == 0) {
+      load_role<D, BF16, MODE>(p, base, gbase, abort_flag, lane);
+    } else if (warp == 1) {
+      mma_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem, lane);
+    }
+  } else {
+    setmaxnreg_inc<REGS_SOFTMAX>();
     softmax_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem, (warp - 4) >> 2, warp & 3, lane);
   }
 
@@ -685,8 +786,8 @@ struct DeviceInfo {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev[64];
 
-int device_info(int& sms) {
-  int dev = 0;
+int device_info(int& sms, int& dev) {
+  dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_DEVICE;
   std::lock_guard<std::mutex> lk(g_dev_mutex);
   DeviceInfo& di = g_dev[dev];
@@ -721,22 +822,27 @@ int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long
 }
 
 template <int D, bool BF16, int MODE>
-int launch(const Params& p, int grid, cudaStream_t st) {
+int launch(const Params& p, int grid, cudaStream_t st, int dev) {
   using L = Layout<D, MODE>;
   auto kern = attn_fwd_kernel<D, BF16, MODE>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
+  static std::atomic<unsigned long long> attr_set{0};  // bit per device
+  const unsigned long long bit = 1ull << dev;
+  if (!(attr_set.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    attr_set.fetch_or(bit);
+  }
   kern<<<grid, NTHREADS, L::SMEM_ALLOC, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D, bool BF16>
-int launch_mode(const Params& p, int mode, int grid, cudaStream_t st) {
+int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev) {
   switch (mode) {
-    case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st);
-    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st);
-    default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st);
+    case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st, dev);
+    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st, dev);
+    default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st, dev);
   }
 }
 
@@ -755,8 +861,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   const long long nqb = (S + UNIT_ROWS - 1) / UNIT_ROWS;
   if ((long long)B * Hq * S > INT_MAX || (long long)B * Hq * nqb > INT_MAX) return ATTN_ERR_INVALID;
 
-  int sms = 0;
-  int rc = device_info(sms);
+  int sms = 0, dev = 0;
+  int rc = device_info(sms, dev);
   if (rc != ATTN_OK) return rc;
 
   Params p;
@@ -787,8 +893,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   const int mode = mask_bits ? MASK_CUSTOM : (causal ? MASK_CAUSAL : MASK_NONE);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (d == 64)
-    return bf16 ? launch_mode<64, true>(p, mode, grid, st) : launch_mode<64, false>(p, mode, grid, st);
-  return bf16 ? launch_mode<128, true>(p, mode, grid, st) : launch_mode<128, false>(p, mode, grid, st);
+    return bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
+  return bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
 }
 
 }  // namespace
