@@ -106,9 +106,10 @@ struct InfoHdr {
 
 struct Params {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps {d, S, B*H}, box {64, 128, 1}, 128B swizzle
+  CUtensorMap tm_m;              // kept-bit words {W4, S, B}, box {4, 256, 1} (custom masks)
   void* o;
   float* lse;
-  const uint32_t* mask;
+  const uint8_t* tflags;  // [B][nqt][nkt] 1 = block holds a kept entry (custom masks)
   uint8_t* visited;
   int B, Hq, Hkv, S, g, nqb, nkt, nqt, W, num_units;
   int causal;
@@ -218,7 +219,6 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
   const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
-  uint32_t* words = reinterpret_cast<uint32_t*>(gbase + L::OFF_WORDS);
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
 
   uint32_t q_empty_par = (1u << L::QBUF) - 1u;  // per Q buffer; "empty" waits start at parity 1
@@ -230,6 +230,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
   uint32_t kpend = 0, kpend_par = 0, vpend = 0, vpend_par = 0;
   int ie = 0;
   uint32_t ie_par = 1;
+  uint32_t ipend = 0, ipend_par = 0;  // descriptor slots with a mask-word load issued
   bool inject = p.inject != 0;
 
   for (int k = 0;; ++k) {
@@ -263,6 +264,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     inject = false;
 
     const int jend = causal ? (last_row(qb, QT - 1, p.S) / BN + 1) : p.nkt;
+    uint32_t f0 = 0, f1 = 0;  // bit (j % 32): Q tile 0 / 1 has a kept entry in key tile j
     for (int j = 0; j < jend; ++j) {
       bool a0 = true;
       bool a1 = (row0 + BM) < p.S;
@@ -270,49 +272,44 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
         a0 = j * BN <= last_row(qb, 0, p.S);
         a1 = a1 && (j * BN <= last_row(qb, 1, p.S));
       }
-      uint32_t w[32];
       if constexpr (MODE == MASK_CUSTOM) {
-        // Kept-bit words of the 256 rows x 4 words of this block: the custom mask ANDed with
-        // the causal bound and the key bound.  Lane l handles word (it*32 + l): row
-        // (it*32 + l) / 4, word (it*32 + l) % 4 -- coalesced 16-byte row segments.
-        uint32_t or0 = 0, or1 = 0;
-#pragma unroll
-        for (int it = 0; it < 32; ++it) {
-          const int idx = it * 32 + lane;
-          const int i = row0 + (idx >> 2);
-          const int gw = j * (BN / 32) + (idx & 3);
-          uint32_t x = 0;
-          if (i < p.S && gw < p.W) {
-            x = __ldg(p.mask + ((size_t)b * p.S + i) * p.W + gw);
-            const int nvalid = p.S - gw * 32;
-            if (nvalid < 32) x &= (1u << nvalid) - 1u;
-            if (causal) {
-              const int lim = i - gw * 32 + 1;
-              x = lim <= 0 ? 0u : (lim < 32 ? (x & ((1u << lim) - 1u)) : x);
-            }
+        // Emptiness bits of the two Q tiles for 32 key tiles at a time, from the map the
+        // mask pre-pass wrote (exact: custom bits AND causal AND key bound).
+        if ((j & 31) == 0) {
+          const int jj = j + lane;
+          const size_t fb = ((size_t)b * p.nqt + qb * QT) * p.nkt;
+          uint32_t x0 = 0, x1 = 0;
+          if (jj < p.nkt) {
+            x0 = p.tflags[fb + jj];
+            if (qb * QT + 1 < p.nqt) x1 = p.tflags[fb + p.nkt + jj];
           }
-          w[it] = x;
-          if (it < 16) or0 |= x; else or1 |= x;
+          f0 = __ballot_sync(0xffffffffu, x0 != 0u);
+          f1 = __ballot_sync(0xffffffffu, x1 != 0u);
         }
-        const bool any0 = __any_sync(0xffffffffu, or0 != 0u);
-        const bool any1 = __any_sync(0xffffffffu, or1 != 0u);
-        a0 = a0 && any0;
-        a1 = a1 && any1;
+        a0 = a0 && ((f0 >> (j & 31)) & 1u);
+        a1 = a1 && ((f1 >> (j & 31)) & 1u);
       }
       if (!a0 && !a1) continue;  // empty block pair: nothing loaded, nothing computed
 
       if (!bwait_warp(bars + 8u * (L::B_IEMPTY + ie), ie_par, abort_flag, to)) goto drain;
-      if constexpr (MODE == MASK_CUSTOM) {
-        uint32_t* dst = words + ie * L::WORDS_PER_ENTRY;
-#pragma unroll
-        for (int it = 0; it < 32; ++it) dst[it * 32 + lane] = w[it];
-      }
       if (lane == 0) {
         hdr[ie].j = j;
         hdr[ie].flags = (a0 ? 1 : 0) | (a1 ? 2 : 0);
+        const uint32_t fb = bars + 8u * (L::B_IFULL + ie);
+        if constexpr (MODE == MASK_CUSTOM) {
+          // the block's kept-bit words (256 rows x 4 words) land in the descriptor slot
+          mbar_expect_tx(fb, L::WORDS_PER_ENTRY * 4);
+          tma_load_3d(base + L::OFF_WORDS + ie * L::WORDS_PER_ENTRY * 4, &p.tm_m, fb,
+                      j * (BN / 32), row0, b);
+        } else {
+          mbar_arrive(fb);
+        }
+      }
+      if constexpr (MODE == MASK_CUSTOM) {
+        ipend |= 1u << ie;
+        ipend_par = (ipend_par & ~(1u << ie)) | ((ie_par ^ 1u) << ie);
       }
       __syncwarp();
-      mbar_arrive(bars + 8u * (L::B_IFULL + ie));
       if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
 
       // K tile j
@@ -347,9 +344,9 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     if (lane == 0) {
       hdr[ie].j = -1;
       hdr[ie].flags = FLAG_END;
+      mbar_arrive(bars + 8u * (L::B_IFULL + ie));
     }
     __syncwarp();
-    mbar_arrive(bars + 8u * (L::B_IFULL + ie));
     if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
   }
   return;
@@ -363,6 +360,8 @@ drain:
       if ((vpend >> s) & 1u) wait_drain(bars + 8u * (L::B_VFULL + s), (vpend_par >> s) & 1u);
     for (int qb2 = 0; qb2 < L::QBUF; ++qb2)
       if ((q_pend >> qb2) & 1u) wait_drain(bars + 8u * (L::B_QFULL + qb2), (q_pend_par >> qb2) & 1u);
+    for (int e = 0; e < NINFO; ++e)
+      if ((ipend >> e) & 1u) wait_drain(bars + 8u * (L::B_IFULL + e), (ipend_par >> e) & 1u);
   }
   __syncwarp();
 }
@@ -706,7 +705,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bars + 8u * (L::B_VEMPTY + s), 1);
     }
     for (int e = 0; e < NINFO; ++e) {
-      mbar_init(bars + 8u * (L::B_IFULL + e), 32);                // the whole load warp
+      mbar_init(bars + 8u * (L::B_IFULL + e), 1);                 // load-warp lane 0
       mbar_init(bars + 8u * (L::B_IEMPTY + e), 1 + QT * BM);      // MMA thread + softmax threads
     }
     for (int t = 0; t < QT; ++t) {
@@ -753,6 +752,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// ------------------------------------------------------------------ custom-mask pre-pass
+// One warp per (batch, 128-row query tile, 128-column key tile) block.  Writes the block's
+// kept-bit words -- the caller's bits AND the key bound (col < S) AND, for causal,
+// col <= row -- into a copy padded to W4 = 4 * nkt words per row, and a 1 into
+// flags[(b*nqt + qt)*nkt + kt] iff any of them is set.  The attention kernel then reads
+// only these: whole word tiles by TMA, and the emptiness flags for its tile skipping.
+__global__ void __launch_bounds__(256) mask_prepass_kernel(const uint32_t* __restrict__ mask,
+                                                           uint32_t* __restrict__ words4,
+                                                           uint8_t* __restrict__ flags, int B,
+                                                           int S, int W, int W4, int nqt, int nkt,
+                                                           int causal) {
+  const long long gw_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw_id >= (long long)B * nqt * nkt) return;  // warp-uniform
+  const int kt = (int)(gw_id % nkt);
+  const long long rest = gw_id / nkt;
+  const int qt = (int)(rest % nqt);
+  const int b = (int)(rest / nqt);
+  uint32_t any = 0;
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int i = qt * BM + rr * 32 + lane;
+    if (i >= S) continue;
+    const uint32_t* src = mask + ((size_t)b * S + i) * W;
+    uint32_t* dst = words4 + ((size_t)b * S + i) * W4;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int gw = kt * 4 + w;
+      uint32_t x = 0;
+      if (gw < W) {
+        x = src[gw];
+        const int nvalid = S - gw * 32;  // >= 1
+        if (nvalid < 32) x &= (1u << nvalid) - 1u;
+        if (causal) {
+          const int lim = i - gw * 32 + 1;
+          x = lim <= 0 ? 0u : (lim < 32 ? (x & ((1u << lim) - 1u)) : x);
+        }
+      }
+      dst[gw] = x;
+      any |= x;
+    }
+  }
+  const bool hit = __any_sync(0xffffffffu, any != 0u);
+  if (lane == 0) flags[gw_id] = hit ? 1 : 0;
 }
 
 }  // namespace attn
@@ -821,6 +866,50 @@ int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Kept-bit words of a custom mask after the pre-pass: 3-D map {W4, S, B} of uint32, box
+// {4 words, 256 rows, 1}: one key tile's words for the 256 rows of a work unit.
+int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int S, int B) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return ATTN_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)W4, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)W4 * 4, (cuuint64_t)S * (cuuint64_t)W4 * 4};
+  cuuint32_t box[3] = {BN / 32, UNIT_ROWS, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(words4), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Scratch of the custom-mask pre-pass: padded kept-bit words [B][S][W4] then the block
+// emptiness flags [B][nqt][nkt].
+struct MaskScratch {
+  size_t words_bytes, flags_bytes;
+  static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+  MaskScratch(int B, int S) {
+    const int nqt = (S + BM - 1) / BM, nkt = (S + BN - 1) / BN;
+    words_bytes = (size_t)B * S * (size_t)(4 * nkt) * 4;
+    flags_bytes = (size_t)B * nqt * nkt;
+  }
+  size_t total() const { return round256(words_bytes) + flags_bytes; }
+};
+
+// Runs the mask pre-pass into `scratch` (MaskScratch layout) and points p at its output.
+int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream_t st) {
+  const MaskScratch ms(p.B, p.S);
+  uint32_t* words4 = reinterpret_cast<uint32_t*>(scratch);
+  uint8_t* flags = reinterpret_cast<uint8_t*>(scratch) + MaskScratch::round256(ms.words_bytes);
+  const int W4 = 4 * p.nkt;
+  const long long warps = (long long)p.B * p.nqt * p.nkt;
+  const long long blocks = (warps * 32 + 255) / 256;
+  if (blocks > INT_MAX) return ATTN_ERR_INVALID;
+  mask_prepass_kernel<<<(unsigned)blocks, 256, 0, st>>>(mask_bits, words4, flags, p.B, p.S, p.W, W4,
+                                                        p.nqt, p.nkt, p.causal);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  p.tflags = flags;
+  return make_mask_map(&p.tm_m, words4, W4, p.S, p.B);
+}
+
 template <int D, bool BF16, int MODE>
 int launch(const Params& p, int grid, cudaStream_t st, int dev) {
   using L = Layout<D, MODE>;
@@ -873,7 +962,6 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   if ((rc = make_map(&p.tm_v, v, bf16, d, S, (long long)B * Hkv)) != ATTN_OK) return rc;
   p.o = o;
   p.lse = lse;
-  p.mask = mask_bits;
   p.visited = visited;
   p.B = B;
   p.Hq = Hq;
@@ -892,9 +980,21 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   const int grid = p.num_units < sms ? p.num_units : sms;
   const int mode = mask_bits ? MASK_CUSTOM : (causal ? MASK_CAUSAL : MASK_NONE);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (d == 64)
-    return bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
-  return bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
+  // Custom masks: stream-ordered scratch for the pre-pass output, freed in stream order
+  // after the launch that reads it.
+  void* scratch = nullptr;
+  if (mode == MASK_CUSTOM) {
+    if (cudaMallocAsync(&scratch, MaskScratch(B, S).total(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = prepare_mask(p, mask_bits, scratch, st);
+  }
+  if (rc == ATTN_OK) {
+    if (d == 64)
+      rc = bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
+    else
+      rc = bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
+  }
+  if (scratch && cudaFreeAsync(scratch, st) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  return rc;
 }
 
 }  // namespace

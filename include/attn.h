@@ -33,7 +33,12 @@
  *   - dtype: ATTN_F16 or ATTN_BF16 (q, k, v and o share it); accumulation is fp32.
  *   - stream: a cudaStream_t (NULL = the legacy default stream).
  *   - Ownership: the caller owns every buffer; the library keeps no pointer
- *     after the call returns and allocates nothing per call.
+ *     after the call returns.  Without a custom mask nothing is allocated.  With
+ *     one, a pre-pass kernel writes the kept-bit words (mask AND causal AND the
+ *     key bound, padded to whole 128-column tiles) and a per-block emptiness map
+ *     into stream-ordered scratch -- cudaMallocAsync / cudaFreeAsync on `stream`,
+ *     B*S*ceil(S/128)*16 + B*ceil(S/128)^2 bytes (plus alignment) -- that the
+ *     attention kernel reads and that is released in stream order after it.
  *   - Errors: arguments are validated before any launch (ATTN_ERR_INVALID /
  *     ATTN_ERR_UNSUPPORTED, nothing launched); a failed launch returns
  *     ATTN_ERR_CUDA.  The work is asynchronous: a kernel that gives up on a
