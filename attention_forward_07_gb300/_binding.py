@@ -24,6 +24,7 @@ _lib = None
 EXPORTS = (
     "attn_fwd",
     "attn_fwd_visited",
+    "attn_fwd_noalloc",
     "attn_check",
     "attn_strerror",
     "attn_tile_shape",
@@ -61,6 +62,8 @@ def library():
         lib.attn_fwd.restype = i
         lib.attn_fwd_visited.argtypes = fwd_args + [p]
         lib.attn_fwd_visited.restype = i
+        lib.attn_fwd_noalloc.argtypes = fwd_args
+        lib.attn_fwd_noalloc.restype = i
         lib.attn_check.argtypes = [p]
         lib.attn_check.restype = i
         lib.attn_strerror.argtypes = [i]
@@ -129,6 +132,14 @@ def attn_fwd_visited(q, k, v, o, lse, mask_bits, causal, scale, visited, stream=
     (query tile, key tile) block the kernel computed; the caller zeroes it first."""
     lib = library()
     _call(lib.attn_fwd_visited, q, k, v, o, lse, mask_bits, causal, scale, stream, extra=(_ptr(visited),))
+
+
+def attn_fwd_noalloc(q, k, v, o, lse=None, mask_bits=None, causal=False, scale=None, stream=None):
+    """attn_fwd for callers that may not allocate device memory: a custom mask's
+    pre-pass output goes into a fixed array the library reserves per GPU (see
+    include/attn.h for the size limit and the rules on sharing it)."""
+    lib = library()
+    _call(lib.attn_fwd_noalloc, q, k, v, o, lse, mask_bits, causal, scale, stream)
 
 
 def attn_check(stream=None) -> int:

@@ -935,9 +935,32 @@ int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev) {
   }
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch for attn_fwd_noalloc: a fixed device array instead of cudaMallocAsync.  In host
+// code the symbol is only a host-side stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device (with that device current) on the
+// first attn_fwd_noalloc call made on it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[64] = {};
+
+int noalloc_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return ATTN_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return ATTN_OK;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
              const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
-             float scale, int dtype, void* stream, uint8_t* visited) {
+             float scale, int dtype, void* stream, uint8_t* visited, bool noalloc = false) {
   // ---- validation (no CUDA call before this block is passed)
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID;
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
@@ -983,8 +1006,16 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
   // Custom masks: stream-ordered scratch for the pre-pass output, freed in stream order
   // after the launch that reads it.
   void* scratch = nullptr;
+  bool owned = false;
   if (mode == MASK_CUSTOM) {
-    if (cudaMallocAsync(&scratch, MaskScratch(B, S).total(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (noalloc) {
+      // the fixed array: reject what does not fit before anything is launched
+      if (MaskScratch(B, S).total() > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID;
+      if ((rc = noalloc_scratch_address(&scratch)) != ATTN_OK) return rc;
+    } else {
+      if (cudaMallocAsync(&scratch, MaskScratch(B, S).total(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+      owned = true;
+    }
     rc = prepare_mask(p, mask_bits, scratch, st);
   }
   if (rc == ATTN_OK) {
@@ -993,7 +1024,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
     else
       rc = bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
   }
-  if (scratch && cudaFreeAsync(scratch, st) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+  if (owned && cudaFreeAsync(scratch, st) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
   return rc;
 }
 
@@ -1016,6 +1047,13 @@ int attn_fwd_visited(const void* q, const void* k, const void* v, void* o, float
   if (!visited) return ATTN_ERR_INVALID;
   return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
                         visited);
+}
+
+int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+                     float scale, int dtype, void* stream) {
+  return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
+                        nullptr, true);
 }
 
 int attn_check(void* stream) {

@@ -90,6 +90,30 @@ int attn_fwd_visited(const void *q, const void *k, const void *v, void *o, float
                      int causal, float scale, int dtype, void *stream, uint8_t *visited);
 
 /*
+ * attn_fwd_noalloc -- attn_fwd for callers that must not allocate device memory:
+ * code running where cudaMalloc / cudaMallocAsync are unavailable or forbidden,
+ * e.g. inside a custom allocator or memory-pool hook (re-entering the allocator
+ * would deadlock or recurse), in real-time paths that may not wait on the
+ * allocator, or in hosts that hand out a fixed memory budget up front.  It takes
+ * the same arguments and computes the same result as attn_fwd.  Without a custom
+ * mask the two are the same call.  With one, the mask pre-pass output goes into a
+ * fixed device array of ATTN_NOALLOC_SCRATCH_BYTES that this library reserves on
+ * every GPU that loads it, held until the process exits, instead of into
+ * stream-ordered scratch; calls whose B*S*ceil(S/128)*16 + B*ceil(S/128)^2
+ * bytes (plus alignment) exceed it return ATTN_ERR_INVALID before any launch.
+ * The first call on a device looks the array's device address up (once, with
+ * that device current); make that first call before any stream capture.  Every
+ * call shares the one array and it keeps the last call's contents (each call
+ * rewrites every byte it then reads, so nothing needs clearing); calls whose
+ * work overlaps on the GPU -- on different streams, say -- race on it, so order
+ * them.  The pages this library follows have no counterpart of this entry point.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
+int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                     const uint32_t *mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
+                     float scale, int dtype, void *stream);
+
+/*
  * attn_check -- synchronise `stream`, then report (and clear) the device status
  * word of the current device: ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if
  * the stream itself reports an error.
