@@ -61,7 +61,7 @@ typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID = -1,     /* a null pointer, a non-positive size, misalignment, bad scale */
-    ATTN_ERR_UNSUPPORTED = -2, /* a head dim or dtype this build has no kernel for */
+    ATTN_ERR_UNSUPPORTED = -2, /* a head dim or dtype the library has no kernel for */
     ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed (launch, tensor map) */
     ATTN_ERR_TIMEOUT = -4,     /* a kernel barrier wait ran out of time; outputs undefined */
     ATTN_ERR_DEVICE = -5       /* no usable sm_103 device */

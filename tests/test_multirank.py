@@ -1,0 +1,51 @@
+"""The N > 1 host logic of bench.py on CPU: two gloo ranks.
+
+Each rank runs its own replica of the workload (weak scaling, no collective on the
+data path); the only cross-rank steps are the barrier and the max over ranks of the
+timed region, which the reported throughput divides by.
+"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    w, r, lr = bench.dist_env()
+    assert (w, r, lr) == (world, rank, rank)
+    bench.barrier(world)
+    t = bench.max_over_ranks(10.0 + rank, world)
+    seeds = [bench.replica_seed(4096, q) for q in range(world)]
+    out[rank] = (t, seeds[rank], len(set(seeds)))
+    dist.destroy_process_group()
+
+
+@pytest.mark.timeout(120)
+def test_two_gloo_ranks_take_the_slowest_time_and_distinct_replicas():
+    world = 2
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+    assert out[0][0] == out[1][0] == 11.0          # max over ranks
+    assert out[0][1] != out[1][1] and out[0][2] == world  # each rank draws its own replica
+
+
+def test_single_rank_defaults():
+    import bench
+    os.environ.pop("WORLD_SIZE", None)
+    assert bench.dist_env()[0] == 1
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.replica_seed(7, 0) == 7
