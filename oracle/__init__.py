@@ -61,6 +61,10 @@ def _load():
             lib.oracle_attn_fwd.restype = i
             lib.oracle_skip_map.argtypes = [p, i, i, i, i, i, p]
             lib.oracle_skip_map.restype = i
+            lib.oracle_attn_rows_ex.argtypes = [p, p, p, i, p, i, i, i, i, i, i, i, i, i, i, d, p, i64, p, p, i]
+            lib.oracle_attn_rows_ex.restype = i
+            lib.oracle_skip_map_ex.argtypes = [p, i, i, i, i, i, i, i, i, i, i, p]
+            lib.oracle_skip_map_ex.restype = i
             lib.oracle_widen.argtypes = [ctypes.c_uint16, i]
             lib.oracle_widen.restype = d
             lib.oracle_num_threads.argtypes = []
@@ -128,6 +132,53 @@ def skip_map(mask_bits, B, S, causal, bm, bn):
     rc = _load().oracle_skip_map(_ptr(mask_bits), B, S, int(bool(causal)), bm, bn, _ptr(out))
     if rc != 0:
         raise RuntimeError(f"oracle_skip_map failed ({rc})")
+    return out
+
+
+def attn_rows_ex(q, k, v, dtype, rows=None, mask_bits=None, mask_per_head=False, causal=False,
+                 window_left=-1, window_right=-1, scale=None, nthreads=0):
+    """Extended definition (see attn_oracle.c): q [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] with Sq <= Sk,
+    bottom-right aligned; optional key band; masks [B,Sq,W] or per head [B,Hq,Sq,W].
+    rows=None evaluates every row and returns O [B,Hq,Sq,d], LSE [B,Hq,Sq]."""
+    for name, a in (("q", q), ("k", k), ("v", v)):
+        if a.dtype != np.uint16 or a.ndim != 4 or not a.flags.c_contiguous:
+            raise ValueError(f"{name} must be a C-contiguous uint16 [B,H,S,d] array")
+    B, Hq, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if mask_bits is not None:
+        mask_bits = np.ascontiguousarray(mask_bits, dtype=np.uint32)
+        want = (B, Hq, Sq, (Sk + 31) // 32) if mask_per_head else (B, Sq, (Sk + 31) // 32)
+        if mask_bits.shape != want:
+            raise ValueError(f"mask_bits shape {mask_bits.shape}, expected {want}")
+    if scale is None:
+        scale = float(np.float32(1.0 / np.sqrt(d)))
+    full = rows is None
+    if full:
+        rows = np.arange(B * Hq * Sq, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    rc = _load().oracle_attn_rows_ex(_ptr(q), _ptr(k), _ptr(v), int(dtype), _ptr(mask_bits), int(bool(mask_per_head)),
+                                     B, Hq, Hkv, Sq, Sk, d, int(bool(causal)), int(window_left), int(window_right),
+                                     float(scale), _ptr(rows), n, _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_rows_ex failed ({rc})")
+    if full:
+        return o.reshape(B, Hq, Sq, d), lse.reshape(B, Hq, Sq)
+    return o, lse
+
+
+def skip_map_ex(mask_bits, mask_per_head, B, Hq, Sq, Sk, causal, window_left, window_right, bm, bn):
+    """uint8 [B*Hm, ceil(Sq/bm), ceil(Sk/bn)], Hm = Hq for per-head masks else 1."""
+    if mask_bits is not None:
+        mask_bits = np.ascontiguousarray(mask_bits, dtype=np.uint32)
+    Hm = Hq if (mask_bits is not None and mask_per_head) else 1
+    out = np.zeros((B * Hm, (Sq + bm - 1) // bm, (Sk + bn - 1) // bn), np.uint8)
+    rc = _load().oracle_skip_map_ex(_ptr(mask_bits), int(bool(mask_per_head)), B, Hq, Sq, Sk, int(bool(causal)),
+                                    int(window_left), int(window_right), bm, bn, _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_skip_map_ex failed ({rc})")
     return out
 
 

@@ -35,6 +35,15 @@
  *   - GQA maps query head hq to key/value head hq / (Hq / Hkv);
  *   - tensors are [B][H][S][d] row-major; LSE is the natural log.
  *
+ * The extended form (oracle_attn_rows_ex) also takes queries and keys of different
+ * lengths Sq <= Sk, aligned at the bottom right (query i sits at key position
+ * i + Sk - Sq, as in prefill against a key/value cache), a band of kept keys around that
+ * position (window_left keys to the left, window_right to the right, -1 = unbounded;
+ * causal is window_right = 0), and custom masks given per query head instead of per
+ * batch entry.  These readings are this library's own extensions (the pages have no
+ * varlen or window masks); with Sq = Sk, no window and shared masks they reduce to the
+ * definition above.
+ *
  * Inputs are the raw 16-bit fp16 / bf16 words; they are widened to double
  * exactly (the oracle consumes the same rounded values the GPU gets).
  * Everything after that is double precision, in the order written above.
@@ -85,6 +94,21 @@ static int allowed(const uint32_t *mask_bits, int b, int i, int j, int S, int ca
         if (((word >> (j % 32)) & 1u) == 0)
             return 0;
     }
+    return 1;
+}
+
+/* The extended rule.  mask_row points at the Sk-bit row of words for (query row i, and
+ * b or b*Hq + hq); pos = i + Sk - Sq. */
+static int allowed_ex(const uint32_t *mask_row, int64_t pos, int64_t j, int causal, int wl, int wr)
+{
+    if (causal && j > pos)
+        return 0;
+    if (wl >= 0 && j < pos - wl)
+        return 0;
+    if (wr >= 0 && j > pos + wr)
+        return 0;
+    if (mask_row && ((mask_row[j / 32] >> (j % 32)) & 1u) == 0)
+        return 0;
     return 1;
 }
 
@@ -226,6 +250,125 @@ int oracle_skip_map(const uint32_t *mask_bits, int B, int S, int causal, int bm,
                             break;
                         }
                 out[((int64_t)b * nqt + qt) * nkt + kt] = (unsigned char)hit;
+            }
+    return 0;
+}
+
+/*
+ * oracle_attn_rows_ex: the extended definition.  q, o: [B][Hq][Sq][d]; k, v:
+ * [B][Hkv][Sk][d]; mask_bits: [B][Sq][ceil(Sk/32)] (mask_per_head = 0) or
+ * [B][Hq][Sq][ceil(Sk/32)] (mask_per_head = 1) or NULL; rows are flat ids
+ * (b*Hq + hq)*Sq + i.  Same outputs as oracle_attn_rows.
+ */
+int oracle_attn_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                        const uint32_t *mask_bits, int mask_per_head, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int d, int causal, int window_left, int window_right,
+                        double scale, const int64_t *rows, int64_t nrows, double *o_out,
+                        double *lse_out, int nthreads)
+{
+    if (!q || !k || !v || !rows || !o_out || !lse_out)
+        return -1;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < Sq || d < 1 || Hq % Hkv != 0)
+        return -1;
+    int64_t total = (int64_t)B * Hq * Sq;
+    for (int64_t r = 0; r < nrows; r++)
+        if (rows[r] < 0 || rows[r] >= total)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    const int64_t W = (Sk + 31) / 32;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)Sk);
+        unsigned char *keep = (unsigned char *)malloc((size_t)Sk);
+        if (!scores || !keep) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < nrows; r++) {
+                const int64_t row_id = rows[r];
+                const int64_t i = row_id % Sq, bh = row_id / Sq, hq = bh % Hq, b = bh / Hq;
+                const int64_t hkv = hq / (Hq / Hkv);
+                const int64_t pos = i + Sk - Sq;
+                const uint16_t *qi = q + ((b * Hq + hq) * Sq + i) * d;
+                const uint16_t *kb = k + (b * Hkv + hkv) * (int64_t)Sk * d;
+                const uint16_t *vb = v + (b * Hkv + hkv) * (int64_t)Sk * d;
+                const uint32_t *mrow = NULL;
+                if (mask_bits)
+                    mrow = mask_bits + ((mask_per_head ? (b * Hq + hq) : b) * Sq + i) * W;
+                double *o_row = o_out + r * d;
+                double m = -INFINITY;
+                int any = 0;
+                for (int64_t j = 0; j < Sk; j++) {
+                    keep[j] = (unsigned char)allowed_ex(mrow, pos, j, causal, window_left, window_right);
+                    if (!keep[j])
+                        continue;
+                    double dot = 0.0;
+                    for (int t = 0; t < d; t++)
+                        dot += widen(qi[t], dtype) * widen(kb[j * d + t], dtype);
+                    scores[j] = scale * dot;
+                    if (scores[j] > m)
+                        m = scores[j];
+                    any = 1;
+                }
+                for (int t = 0; t < d; t++)
+                    o_row[t] = 0.0;
+                if (!any) {
+                    lse_out[r] = -INFINITY;
+                    continue;
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j < Sk; j++) {
+                    if (!keep[j])
+                        continue;
+                    double w = exp(scores[j] - m);
+                    l += w;
+                    for (int t = 0; t < d; t++)
+                        o_row[t] += w * widen(vb[j * d + t], dtype);
+                }
+                for (int t = 0; t < d; t++)
+                    o_row[t] /= l;
+                lse_out[r] = m + log(l);
+            }
+        }
+        free(scores);
+        free(keep);
+    }
+    return failed ? -2 : 0;
+}
+
+/*
+ * oracle_skip_map_ex: block emptiness under the extended rule, out [B*Hm][nqt][nkt] with
+ * Hm = Hq if mask_per_head else 1, nqt = ceil(Sq/bm), nkt = ceil(Sk/bn).
+ */
+int oracle_skip_map_ex(const uint32_t *mask_bits, int mask_per_head, int B, int Hq, int Sq, int Sk,
+                       int causal, int window_left, int window_right, int bm, int bn,
+                       unsigned char *out)
+{
+    if (!out || B < 1 || Sq < 1 || Sk < Sq || bm < 1 || bn < 1)
+        return -1;
+    const int nqt = (Sq + bm - 1) / bm, nkt = (Sk + bn - 1) / bn;
+    const int Hm = (mask_bits && mask_per_head) ? Hq : 1;
+    const int64_t W = (Sk + 31) / 32;
+    for (int64_t bh = 0; bh < (int64_t)B * Hm; bh++)
+        for (int qt = 0; qt < nqt; qt++)
+            for (int kt = 0; kt < nkt; kt++) {
+                int hit = 0;
+                for (int64_t i = (int64_t)qt * bm; i < Sq && i < (int64_t)(qt + 1) * bm && !hit; i++) {
+                    const uint32_t *mrow = mask_bits ? mask_bits + (bh * Sq + i) * W : NULL;
+                    for (int64_t j = (int64_t)kt * bn; j < Sk && j < (int64_t)(kt + 1) * bn; j++)
+                        if (allowed_ex(mrow, i + Sk - Sq, j, causal, window_left, window_right)) {
+                            hit = 1;
+                            break;
+                        }
+                }
+                out[(bh * nqt + qt) * nkt + kt] = (unsigned char)hit;
             }
     return 0;
 }
