@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     AttnError,
     attn_check,
     attn_fwd,
+    attn_fwd_ex,
     attn_fwd_noalloc,
     attn_fwd_visited,
     attn_strerror,

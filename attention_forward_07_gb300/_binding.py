@@ -25,6 +25,7 @@ EXPORTS = (
     "attn_fwd",
     "attn_fwd_visited",
     "attn_fwd_noalloc",
+    "attn_fwd_ex",
     "attn_check",
     "attn_strerror",
     "attn_tile_shape",
@@ -32,6 +33,16 @@ EXPORTS = (
     "attn_debug_inject",
     "attn_version",
 )
+
+
+class FwdParams(ctypes.Structure):
+    """attn_fwd_params_t of include/attn.h."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("o", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p), ("mask_bits", ctypes.c_void_p), ("mask_per_head", ctypes.c_int),
+                ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Sq", ctypes.c_int),
+                ("Sk", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int), ("window_left", ctypes.c_int),
+                ("window_right", ctypes.c_int), ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
+                ("stream", ctypes.c_void_p), ("visited", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -64,6 +75,8 @@ def library():
         lib.attn_fwd_visited.restype = i
         lib.attn_fwd_noalloc.argtypes = fwd_args
         lib.attn_fwd_noalloc.restype = i
+        lib.attn_fwd_ex.argtypes = [ctypes.POINTER(FwdParams)]
+        lib.attn_fwd_ex.restype = i
         lib.attn_check.argtypes = [p]
         lib.attn_check.restype = i
         lib.attn_strerror.argtypes = [i]
@@ -140,6 +153,27 @@ def attn_fwd_noalloc(q, k, v, o, lse=None, mask_bits=None, causal=False, scale=N
     include/attn.h for the size limit and the rules on sharing it)."""
     lib = library()
     _call(lib.attn_fwd_noalloc, q, k, v, o, lse, mask_bits, causal, scale, stream)
+
+
+def attn_fwd_ex(q, k, v, o, lse=None, mask_bits=None, mask_per_head=False, causal=False, window_left=-1,
+                window_right=-1, scale=None, visited=None, stream=None):
+    """Generalised forward: q/o [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] with Sk >= Sq (bottom-right
+    aligned), a band of kept keys (window_left / window_right, -1 = unbounded), custom masks
+    [B,Sq,ceil(Sk/32)] or per head [B,Hq,Sq,ceil(Sk/32)]; see include/attn.h."""
+    B, Hq, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    prm = FwdParams(q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), o=o.data_ptr(),
+                    lse=None if lse is None else lse.data_ptr(),
+                    mask_bits=None if mask_bits is None else mask_bits.data_ptr(),
+                    mask_per_head=int(bool(mask_per_head)), B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d,
+                    causal=int(bool(causal)), window_left=int(window_left), window_right=int(window_right),
+                    scale=float(scale), dtype=_dtype_code(q), stream=_stream_handle(stream).value,
+                    visited=None if visited is None else visited.data_ptr())
+    rc = library().attn_fwd_ex(ctypes.byref(prm))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_ex")
 
 
 def attn_check(stream=None) -> int:

@@ -59,7 +59,9 @@ constexpr int O_COL0 = 256;    // O_t (fp32, d columns) at 256 + t*128
 constexpr int FLAG_END = 4;    // info entry marking the end of a work unit
 constexpr float LN2 = 0.69314718055994530942f;
 
-enum MaskMode { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_CUSTOM = 2 };
+// NONE: every key; BAND: keys in [key_lo(i), key_hi(i)) per query row (causal, sliding
+// windows); CUSTOM: kept-bit words from the mask pre-pass (which folds the band in).
+enum MaskMode { MASK_NONE = 0, MASK_BAND = 1, MASK_CUSTOM = 2 };
 
 template <int D, int MODE>
 struct Layout {
@@ -111,8 +113,12 @@ struct Params {
   float* lse;
   const uint8_t* tflags;  // [B][nqt][nkt] 1 = block holds a kept entry (custom masks)
   uint8_t* visited;
-  int B, Hq, Hkv, S, g, nqb, nkt, nqt, W, num_units;
-  int causal;
+  int B, Hq, Hkv, Sq, Sk, g, nqb, nkt, nqt, W, num_units;
+  // Query row i sits at key position i + off (off = Sk - Sq, bottom-right alignment); the
+  // band keeps keys with pos - wl <= key <= pos + er (wl / er = -1: unbounded).
+  int off, wl, er;
+  int mask_heads;  // custom-mask rows per batch entry: Hq (per-head masks) or 1
+  int causal;      // the band only bounds keys on the right: longest units first
   int inject;
   float scale_log2;
   unsigned long long timeout_ns;
@@ -191,9 +197,12 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
   }
 }
 
-// Last query row (inclusive, clipped to S-1) of Q tile t of block qb.
-__device__ __forceinline__ int last_row(int qb, int t, int S) {
-  return min(qb * UNIT_ROWS + t * BM + BM - 1, S - 1);
+// Kept keys of query row i under the band: [key_lo, key_hi).
+__device__ __forceinline__ int key_lo(const Params& p, int i) {
+  return p.wl < 0 ? 0 : max(0, i + p.off - p.wl);
+}
+__device__ __forceinline__ int key_hi(const Params& p, int i) {
+  return p.er < 0 ? p.Sk : min(p.Sk, i + p.off + p.er + 1);
 }
 
 }  // namespace attn
@@ -216,7 +225,7 @@ template <int D, bool BF16, int MODE>
 __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_t* gbase,
                                           volatile int* abort_flag, int lane) {
   using L = Layout<D, MODE>;
-  const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
+  const bool causal = p.causal != 0;
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -263,21 +272,28 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     }
     inject = false;
 
-    const int jend = causal ? (last_row(qb, QT - 1, p.S) / BN + 1) : p.nkt;
+    // Key-tile range of each Q tile under the band (key_lo / key_hi grow with the row).
+    int jlo[QT], jhi[QT];
+#pragma unroll
+    for (int t = 0; t < QT; ++t) {
+      const int r0 = row0 + t * BM;
+      const int r1 = min(r0 + BM - 1, p.Sq - 1);
+      jlo[t] = key_lo(p, r0) / BN;
+      jhi[t] = r0 < p.Sq ? (key_hi(p, r1) - 1) / BN : -1;  // -1: no such Q tile
+    }
+    const int jbeg = (jhi[1] >= 0) ? min(jlo[0], jlo[1]) : jlo[0];
+    const int jend = max(jhi[0], jhi[1]) + 1;
+    const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
     uint32_t f0 = 0, f1 = 0;  // bit (j % 32): Q tile 0 / 1 has a kept entry in key tile j
-    for (int j = 0; j < jend; ++j) {
-      bool a0 = true;
-      bool a1 = (row0 + BM) < p.S;
-      if (causal) {
-        a0 = j * BN <= last_row(qb, 0, p.S);
-        a1 = a1 && (j * BN <= last_row(qb, 1, p.S));
-      }
+    for (int j = jbeg; j < jend; ++j) {
+      bool a0 = j >= jlo[0] && j <= jhi[0];
+      bool a1 = j >= jlo[1] && j <= jhi[1];
       if constexpr (MODE == MASK_CUSTOM) {
         // Emptiness bits of the two Q tiles for 32 key tiles at a time, from the map the
         // mask pre-pass wrote (exact: custom bits AND causal AND key bound).
-        if ((j & 31) == 0) {
-          const int jj = j + lane;
-          const size_t fb = ((size_t)b * p.nqt + qb * QT) * p.nkt;
+        if (j == jbeg || (j & 31) == 0) {
+          const int jj = (j & ~31) + lane;
+          const size_t fb = ((size_t)mb * p.nqt + qb * QT) * p.nkt;
           uint32_t x0 = 0, x1 = 0;
           if (jj < p.nkt) {
             x0 = p.tflags[fb + jj];
@@ -300,7 +316,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
           // the block's kept-bit words (256 rows x 4 words) land in the descriptor slot
           mbar_expect_tx(fb, L::WORDS_PER_ENTRY * 4);
           tma_load_3d(base + L::OFF_WORDS + ie * L::WORDS_PER_ENTRY * 4, &p.tm_m, fb,
-                      j * (BN / 32), row0, b);
+                      j * (BN / 32), row0, mb);
         } else {
           mbar_arrive(fb);
         }
@@ -382,7 +398,7 @@ template <int D, bool BF16, int MODE>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t* gbase,
                                          volatile int* abort_flag, uint32_t tmem, int lane) {
   using L = Layout<D, MODE>;
-  const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
+  const bool causal = p.causal != 0;
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -500,7 +516,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
                                              int quarter, int lane) {
   using L = Layout<D, MODE>;
   using OutT = uint16_t;
-  const bool causal = (MODE == MASK_CAUSAL) || (MODE == MASK_CUSTOM && p.causal);
+  const bool causal = p.causal != 0;
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
   const uint32_t* words = reinterpret_cast<const uint32_t*>(gbase + L::OFF_WORDS);
@@ -549,9 +565,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       tmem_ld32x32b_x64(s_addr + 64, sb);
 
       // Mask: excluded scores become -inf (weight exactly 0).
-      int lim = p.S - j * BN;  // keys at or past S
-      if (MODE == MASK_CAUSAL) lim = min(lim, i - j * BN + 1);
-      const bool edge = (MODE != MASK_CUSTOM) && __any_sync(0xffffffffu, lim < BN);
+      // band / key bound: kept columns of this tile are [lo, hi) relative to its first key
+      const int hi = (MODE == MASK_NONE ? p.Sk : key_hi(p, i)) - j * BN;
+      const int lo = (MODE == MASK_NONE ? 0 : key_lo(p, i)) - j * BN;
+      const bool edge = (MODE != MASK_CUSTOM) && __any_sync(0xffffffffu, hi < BN || lo > 0);
       const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
       auto mask_half = [&](uint32_t(&h)[64], int c0) {
         if constexpr (MODE == MASK_CUSTOM) {
@@ -561,7 +578,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
         } else if (edge) {
 #pragma unroll
           for (int cc = 0; cc < 64; ++cc)
-            if (c0 + cc >= lim) h[cc] = __float_as_uint(-INFINITY);
+            if (c0 + cc >= hi || c0 + cc < lo) h[cc] = __float_as_uint(-INFINITY);
         }
       };
       // Row max of one half: four independent 3-input max chains, chain x over h[16x, 16x+16).
@@ -651,9 +668,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       o_par ^= 1u;
       tc_fence_after();
     }
-    const bool row_ok = i < p.S;
+    const bool row_ok = i < p.Sq;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.S + (row_ok ? i : 0)) * D;
+    OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + (row_ok ? i : 0)) * D;
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t ob[32];
@@ -674,7 +691,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       }
     }
     if (row_ok && p.lse)
-      p.lse[(size_t)(b * p.Hq + hq) * p.S + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+      p.lse[(size_t)(b * p.Hq + hq) * p.Sq + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
   }
 }
 
@@ -755,43 +772,47 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
 }
 
 // ------------------------------------------------------------------ custom-mask pre-pass
-// One warp per (batch, 128-row query tile, 128-column key tile) block.  Writes the block's
-// kept-bit words -- the caller's bits AND the key bound (col < S) AND, for causal,
-// col <= row -- into a copy padded to W4 = 4 * nkt words per row, and a 1 into
-// flags[(b*nqt + qt)*nkt + kt] iff any of them is set.  The attention kernel then reads
-// only these: whole word tiles by TMA, and the emptiness flags for its tile skipping.
+// Bits lo .. hi-1 of a 32-bit word (clipped to the word).
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t upto_hi = hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  const uint32_t below_lo = (1u << lo) - 1u;
+  return upto_hi & ~below_lo;
+}
+
+// One warp per (mask row block mb = batch or batch*Hq + head, 128-row query tile, 128-key
+// tile).  Writes the block's kept-bit words -- the caller's bits AND the key bound
+// (key < Sk) AND the band [key_lo(i), key_hi(i)) -- into a copy padded to W4 = 4 * nkt words
+// per row, and a 1 into flags[(mb*nqt + qt)*nkt + kt] iff any of them is set.  The attention
+// kernel then reads only these: whole word tiles by TMA, and the emptiness flags for its
+// tile skipping.
 __global__ void __launch_bounds__(256) mask_prepass_kernel(const uint32_t* __restrict__ mask,
                                                            uint32_t* __restrict__ words4,
-                                                           uint8_t* __restrict__ flags, int B,
-                                                           int S, int W, int W4, int nqt, int nkt,
-                                                           int causal) {
+                                                           uint8_t* __restrict__ flags, Params p,
+                                                           int nmb) {
   const long long gw_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (gw_id >= (long long)B * nqt * nkt) return;  // warp-uniform
-  const int kt = (int)(gw_id % nkt);
-  const long long rest = gw_id / nkt;
-  const int qt = (int)(rest % nqt);
-  const int b = (int)(rest / nqt);
+  if (gw_id >= (long long)nmb * p.nqt * p.nkt) return;  // warp-uniform
+  const int kt = (int)(gw_id % p.nkt);
+  const long long rest = gw_id / p.nkt;
+  const int qt = (int)(rest % p.nqt);
+  const long long mbk = rest / p.nqt;
+  const int W4 = 4 * p.nkt;
   uint32_t any = 0;
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
     const int i = qt * BM + rr * 32 + lane;
-    if (i >= S) continue;
-    const uint32_t* src = mask + ((size_t)b * S + i) * W;
-    uint32_t* dst = words4 + ((size_t)b * S + i) * W4;
+    if (i >= p.Sq) continue;
+    const uint32_t* src = mask + ((size_t)mbk * p.Sq + i) * p.W;
+    uint32_t* dst = words4 + ((size_t)mbk * p.Sq + i) * W4;
+    const int klo = key_lo(p, i), khi = key_hi(p, i);  // khi <= Sk
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const int gw = kt * 4 + w;
       uint32_t x = 0;
-      if (gw < W) {
-        x = src[gw];
-        const int nvalid = S - gw * 32;  // >= 1
-        if (nvalid < 32) x &= (1u << nvalid) - 1u;
-        if (causal) {
-          const int lim = i - gw * 32 + 1;
-          x = lim <= 0 ? 0u : (lim < 32 ? (x & ((1u << lim) - 1u)) : x);
-        }
-      }
+      if (gw < p.W) x = src[gw] & bit_range(klo - gw * 32, khi - gw * 32);
       dst[gw] = x;
       any |= x;
     }
@@ -868,11 +889,11 @@ int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long
 
 // Kept-bit words of a custom mask after the pre-pass: 3-D map {W4, S, B} of uint32, box
 // {4 words, 256 rows, 1}: one key tile's words for the 256 rows of a work unit.
-int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int S, int B) {
+int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nmb) {
   auto enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
-  cuuint64_t dims[3] = {(cuuint64_t)W4, (cuuint64_t)S, (cuuint64_t)B};
-  cuuint64_t strides[2] = {(cuuint64_t)W4 * 4, (cuuint64_t)S * (cuuint64_t)W4 * 4};
+  cuuint64_t dims[3] = {(cuuint64_t)W4, (cuuint64_t)Sq, (cuuint64_t)nmb};
+  cuuint64_t strides[2] = {(cuuint64_t)W4 * 4, (cuuint64_t)Sq * (cuuint64_t)W4 * 4};
   cuuint32_t box[3] = {BN / 32, UNIT_ROWS, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(words4), dims, strides,
@@ -881,33 +902,33 @@ int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int S, int B) 
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Scratch of the custom-mask pre-pass: padded kept-bit words [B][S][W4] then the block
-// emptiness flags [B][nqt][nkt].
+// Scratch of the custom-mask pre-pass for nmb mask row blocks (B, or B*Hq for per-head
+// masks): padded kept-bit words [nmb][Sq][W4] then the block emptiness flags
+// [nmb][nqt][nkt].
 struct MaskScratch {
   size_t words_bytes, flags_bytes;
   static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
-  MaskScratch(int B, int S) {
-    const int nqt = (S + BM - 1) / BM, nkt = (S + BN - 1) / BN;
-    words_bytes = (size_t)B * S * (size_t)(4 * nkt) * 4;
-    flags_bytes = (size_t)B * nqt * nkt;
+  MaskScratch(long long nmb, int Sq, int Sk) {
+    const long long nqt = (Sq + BM - 1) / BM, nkt = (Sk + BN - 1) / BN;
+    words_bytes = (size_t)nmb * Sq * (size_t)(4 * nkt) * 4;
+    flags_bytes = (size_t)(nmb * nqt * nkt);
   }
   size_t total() const { return round256(words_bytes) + flags_bytes; }
 };
 
 // Runs the mask pre-pass into `scratch` (MaskScratch layout) and points p at its output.
 int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream_t st) {
-  const MaskScratch ms(p.B, p.S);
+  const int nmb = p.B * p.mask_heads;
+  const MaskScratch ms(nmb, p.Sq, p.Sk);
   uint32_t* words4 = reinterpret_cast<uint32_t*>(scratch);
   uint8_t* flags = reinterpret_cast<uint8_t*>(scratch) + MaskScratch::round256(ms.words_bytes);
-  const int W4 = 4 * p.nkt;
-  const long long warps = (long long)p.B * p.nqt * p.nkt;
+  const long long warps = (long long)nmb * p.nqt * p.nkt;
   const long long blocks = (warps * 32 + 255) / 256;
   if (blocks > INT_MAX) return ATTN_ERR_INVALID;
-  mask_prepass_kernel<<<(unsigned)blocks, 256, 0, st>>>(mask_bits, words4, flags, p.B, p.S, p.W, W4,
-                                                        p.nqt, p.nkt, p.causal);
+  mask_prepass_kernel<<<(unsigned)blocks, 256, 0, st>>>(mask_bits, words4, flags, p, nmb);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   p.tflags = flags;
-  return make_mask_map(&p.tm_m, words4, W4, p.S, p.B);
+  return make_mask_map(&p.tm_m, words4, 4 * p.nkt, p.Sq, nmb);
 }
 
 template <int D, bool BF16, int MODE>
@@ -930,7 +951,7 @@ template <int D, bool BF16>
 int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev) {
   switch (mode) {
     case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st, dev);
-    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st, dev);
+    case MASK_BAND: return launch<D, BF16, MASK_BAND>(p, grid, st, dev);
     default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st, dev);
   }
 }
@@ -958,20 +979,22 @@ int noalloc_scratch_address(void** out) {
   return ATTN_OK;
 }
 
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
-             const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
-             float scale, int dtype, void* stream, uint8_t* visited, bool noalloc = false) {
+int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // ---- validation (no CUDA call before this block is passed)
-  if (!q || !k || !v || !o) return ATTN_ERR_INVALID;
-  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID;
-  const uintptr_t a16 = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)o;
+  if (!a.q || !a.k || !a.v || !a.o) return ATTN_ERR_INVALID;
+  if (a.B < 1 || a.Hq < 1 || a.Hkv < 1 || a.Sq < 1 || a.Sk < a.Sq || a.Hq % a.Hkv != 0)
+    return ATTN_ERR_INVALID;
+  if (a.window_left < -1 || a.window_right < -1) return ATTN_ERR_INVALID;
+  if (a.mask_per_head != 0 && a.mask_per_head != 1) return ATTN_ERR_INVALID;
+  if (a.d != 64 && a.d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (a.dtype != ATTN_F16 && a.dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (!(a.scale > 0.f) || !std::isfinite(a.scale)) return ATTN_ERR_INVALID;
+  const uintptr_t a16 = (uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o;
   if (a16 & 15u) return ATTN_ERR_INVALID;
-  if (((uintptr_t)lse & 3u) || ((uintptr_t)mask_bits & 3u)) return ATTN_ERR_INVALID;
-  const long long nqb = (S + UNIT_ROWS - 1) / UNIT_ROWS;
-  if ((long long)B * Hq * S > INT_MAX || (long long)B * Hq * nqb > INT_MAX) return ATTN_ERR_INVALID;
+  if (((uintptr_t)a.lse & 3u) || ((uintptr_t)a.mask_bits & 3u)) return ATTN_ERR_INVALID;
+  const long long nqb = (a.Sq + UNIT_ROWS - 1) / UNIT_ROWS;
+  if ((long long)a.B * a.Hq * a.Sk > INT_MAX || (long long)a.B * a.Hq * nqb > INT_MAX)
+    return ATTN_ERR_INVALID;
 
   int sms = 0, dev = 0;
   int rc = device_info(sms, dev);
@@ -979,53 +1002,87 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
 
   Params p;
   std::memset(&p, 0, sizeof p);
-  const bool bf16 = dtype == ATTN_BF16;
-  if ((rc = make_map(&p.tm_q, q, bf16, d, S, (long long)B * Hq)) != ATTN_OK) return rc;
-  if ((rc = make_map(&p.tm_k, k, bf16, d, S, (long long)B * Hkv)) != ATTN_OK) return rc;
-  if ((rc = make_map(&p.tm_v, v, bf16, d, S, (long long)B * Hkv)) != ATTN_OK) return rc;
-  p.o = o;
-  p.lse = lse;
-  p.visited = visited;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.S = S;
-  p.g = Hq / Hkv;
+  const bool bf16 = a.dtype == ATTN_BF16;
+  if ((rc = make_map(&p.tm_q, a.q, bf16, a.d, a.Sq, (long long)a.B * a.Hq)) != ATTN_OK) return rc;
+  if ((rc = make_map(&p.tm_k, a.k, bf16, a.d, a.Sk, (long long)a.B * a.Hkv)) != ATTN_OK) return rc;
+  if ((rc = make_map(&p.tm_v, a.v, bf16, a.d, a.Sk, (long long)a.B * a.Hkv)) != ATTN_OK) return rc;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.visited = a.visited;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.g = a.Hq / a.Hkv;
   p.nqb = (int)nqb;
-  p.nkt = (S + BN - 1) / BN;
-  p.nqt = (S + BM - 1) / BM;
-  p.W = (S + 31) / 32;
-  p.num_units = B * Hq * (int)nqb;
-  p.causal = causal ? 1 : 0;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.nkt = (a.Sk + BN - 1) / BN;
+  p.nqt = (a.Sq + BM - 1) / BM;
+  p.W = (a.Sk + 31) / 32;
+  p.num_units = a.B * a.Hq * (int)nqb;
+  p.off = a.Sk - a.Sq;
+  p.wl = a.window_left;
+  p.er = a.causal ? 0 : a.window_right;  // causal: nothing right of the aligned position
+  p.mask_heads = (a.mask_bits && a.mask_per_head) ? a.Hq : 1;
+  p.causal = (p.er >= 0 && p.wl < 0) ? 1 : 0;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.exchange(0);
   const int grid = p.num_units < sms ? p.num_units : sms;
-  const int mode = mask_bits ? MASK_CUSTOM : (causal ? MASK_CAUSAL : MASK_NONE);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int mode = a.mask_bits ? MASK_CUSTOM : ((p.wl >= 0 || p.er >= 0) ? MASK_BAND : MASK_NONE);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(a.stream);
   // Custom masks: stream-ordered scratch for the pre-pass output, freed in stream order
   // after the launch that reads it.
   void* scratch = nullptr;
   bool owned = false;
   if (mode == MASK_CUSTOM) {
+    const size_t need = MaskScratch((long long)a.B * p.mask_heads, a.Sq, a.Sk).total();
     if (noalloc) {
       // the fixed array: reject what does not fit before anything is launched
-      if (MaskScratch(B, S).total() > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID;
+      if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID;
       if ((rc = noalloc_scratch_address(&scratch)) != ATTN_OK) return rc;
     } else {
-      if (cudaMallocAsync(&scratch, MaskScratch(B, S).total(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+      if (cudaMallocAsync(&scratch, need, st) != cudaSuccess) return ATTN_ERR_CUDA;
       owned = true;
     }
-    rc = prepare_mask(p, mask_bits, scratch, st);
+    rc = prepare_mask(p, a.mask_bits, scratch, st);
   }
   if (rc == ATTN_OK) {
-    if (d == 64)
+    if (a.d == 64)
       rc = bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
     else
       rc = bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
   }
   if (owned && cudaFreeAsync(scratch, st) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
   return rc;
+}
+
+attn_fwd_params_t square_params(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d,
+                                int causal, float scale, int dtype, void* stream, uint8_t* visited) {
+  attn_fwd_params_t a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.mask_bits = mask_bits;
+  a.mask_per_head = 0;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sq = S;
+  a.Sk = S;
+  a.d = d;
+  a.causal = causal;
+  a.window_left = -1;
+  a.window_right = -1;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.stream = stream;
+  a.visited = visited;
+  return a;
 }
 
 }  // namespace
@@ -1037,23 +1094,29 @@ extern "C" {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
              float scale, int dtype, void* stream) {
-  return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
-                        nullptr);
+  return attn::fwd_impl(attn::square_params(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal,
+                                            scale, dtype, stream, nullptr));
+}
+
+int attn_fwd_ex(const attn_fwd_params_t* params) {
+  if (!params) return ATTN_ERR_INVALID;
+  return attn::fwd_impl(*params);
 }
 
 int attn_fwd_visited(const void* q, const void* k, const void* v, void* o, float* lse,
                      const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
                      float scale, int dtype, void* stream, uint8_t* visited) {
   if (!visited) return ATTN_ERR_INVALID;
-  return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
-                        visited);
+  return attn::fwd_impl(attn::square_params(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal,
+                                            scale, dtype, stream, visited));
 }
 
 int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                      const uint32_t* mask_bits, int B, int Hq, int Hkv, int S, int d, int causal,
                      float scale, int dtype, void* stream) {
-  return attn::fwd_impl(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal, scale, dtype, stream,
-                        nullptr, true);
+  return attn::fwd_impl(attn::square_params(q, k, v, o, lse, mask_bits, B, Hq, Hkv, S, d, causal,
+                                            scale, dtype, stream, nullptr),
+                        true);
 }
 
 int attn_check(void* stream) {

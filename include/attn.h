@@ -76,6 +76,39 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              float scale, int dtype, void *stream);
 
 /*
+ * attn_fwd_ex -- the same computation with the generalisations a prefill against a
+ * key/value cache and local attention need (the pages themselves stop at Sq = Sk and the
+ * masks above; these follow the same tile, bit-word and skip path):
+ *   - Sq query rows against Sk >= Sq keys, aligned at the bottom right: query i sits at
+ *     key position pos(i) = i + Sk - Sq.  q, o: [B][Hq][Sq][d]; k, v: [B][Hkv][Sk][d];
+ *     lse: [B][Hq][Sq].
+ *   - a band of kept keys: pos(i) - window_left <= j <= pos(i) + window_right
+ *     (-1 = unbounded on that side); causal = 1 keeps j <= pos(i) (window_right is then
+ *     treated as 0).
+ *   - custom masks of [B][Sq][ceil(Sk/32)] words (mask_per_head = 0) or
+ *     [B][Hq][Sq][ceil(Sk/32)] (mask_per_head = 1), ANDed with the band.
+ *   - visited: as for attn_fwd_visited (nqt = ceil(Sq/bm), nkt = ceil(Sk/bn)), or NULL.
+ * With Sq = Sk = S, windows -1 and mask_per_head = 0 it is attn_fwd.  Custom masks take
+ * stream-ordered scratch of nm*Sq*ceil(Sk/128)*16 + nm*ceil(Sq/128)*ceil(Sk/128) bytes,
+ * nm = B (or B*Hq per head).  Errors as for attn_fwd; Sk < Sq is ATTN_ERR_INVALID.
+ */
+typedef struct {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    const uint32_t *mask_bits;
+    int mask_per_head;
+    int B, Hq, Hkv, Sq, Sk, d;
+    int causal, window_left, window_right;
+    float scale;
+    int dtype;
+    void *stream;
+    uint8_t *visited;
+} attn_fwd_params_t;
+
+int attn_fwd_ex(const attn_fwd_params_t *params);
+
+/*
  * attn_fwd_visited -- attn_fwd that also records which (query tile, key tile)
  * blocks it computed: visited[((b*Hq + hq)*nqt + qt)*nkt + kt] = 1, uint8,
  * device memory, nqt = ceil(S/bm), nkt = ceil(S/bn) with (bm, bn) from

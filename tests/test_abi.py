@@ -95,3 +95,14 @@ def test_hooks(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_call_without_device_reports_device_error(lib):
     assert _fwd(lib) == -5
+
+
+def test_fwd_ex_validation(lib):
+    from attention_forward_07_gb300._binding import FwdParams
+    assert lib.attn_fwd_ex(None) == -1
+    base = dict(q=P, k=P, v=P, o=P, B=1, Hq=2, Hkv=2, Sq=128, Sk=256, d=64, causal=1, window_left=-1,
+                window_right=-1, scale=0.125, dtype=0)
+    for kw, status in ((dict(Sk=64), -1), (dict(window_left=-2), -1), (dict(window_right=-5), -1),
+                       (dict(mask_per_head=2), -1), (dict(d=80), -2), (dict(Sq=0), -1)):
+        args = dict(base, **kw)
+        assert lib.attn_fwd_ex(ctypes.byref(FwdParams(**args))) == status, kw

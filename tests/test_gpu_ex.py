@@ -1,0 +1,82 @@
+"""attn_fwd_ex against the oracle's extended definition: Sq < Sk bottom-right aligned,
+sliding-window bands, per-head custom masks, and the tile-skip map under them."""
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_07_gb300 as af
+import oracle
+from attention_forward_07_gb300 import inputs as inp
+
+from gpu_util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, bits, per_head, causal, wl, wr, scale, visited=False):
+    dev = "cuda"
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if bits is None else torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(dev)
+    B, Hq, Sq, d = q.shape
+    Sk = k.shape[2]
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device=dev)
+    vis = torch.zeros((B, Hq, -(-Sq // 128), -(-Sk // 128)), dtype=torch.uint8, device=dev) if visited else None
+    af.attn_fwd_ex(qd, kd, vd, o, lse, md, per_head, causal, wl, wr, scale, vis)
+    af.attn_check()
+    out = (o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
+    return out + ((vis.cpu().numpy(),) if visited else ())
+
+
+CASES = [
+    # B, Hq, Hkv, Sq, Sk, d, dtype, causal, wl, wr, mask
+    (2, 4, 2, 200, 500, 128, inp.BF16, True, -1, -1, None),        # prefill against a cache
+    (1, 2, 2, 1, 300, 64, inp.F16, True, -1, -1, None),            # one new query
+    (1, 3, 3, 257, 257, 128, inp.BF16, True, 100, -1, None),       # causal sliding window
+    (2, 2, 1, 700, 700, 64, inp.F16, False, 50, 30, None),         # symmetric-ish band
+    (1, 2, 2, 300, 900, 128, inp.BF16, False, 200, 40, None),      # band with Sq < Sk
+    (2, 4, 2, 256, 384, 64, inp.F16, True, -1, -1, "shared"),      # custom mask, Sq < Sk
+    (2, 4, 2, 300, 300, 128, inp.BF16, True, 120, -1, "head"),     # per-head mask + window
+    (1, 4, 4, 129, 640, 64, inp.F16, False, -1, -1, "head"),       # per-head, ragged
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}_Hq{}_Hkv{}_Sq{}_Sk{}_d{}_c{}_w{}_{}_{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], int(c[7]), c[8], c[9], c[10]))
+def test_extended_parity_and_skip_map(case):
+    B, Hq, Hkv, Sq, Sk, d, dtype, causal, wl, wr, mask = case
+    q, k, v = inp.qkv(B, Hq, Hkv, Sk, d, dtype, Sq + Sk)
+    q = q[:, :, :Sq].contiguous()
+    per_head = mask == "head"
+    bits = None
+    if mask == "shared":
+        bits = inp.pack_bits(inp.bernoulli_mask(B, Sk, 3)[:, :Sq])
+    elif mask == "head":
+        keep = inp.bernoulli_mask(B * Hq, Sk, 4)[:, :Sq]
+        bits = inp.pack_bits(keep).reshape(B, Hq, Sq, -1)
+    scale = 1.0 / d ** 0.5
+    o, lse, vis = _run(q, k, v, bits, per_head, causal, wl, wr, scale, visited=True)
+    o_ref, lse_ref = oracle.attn_rows_ex(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), dtype, None, bits,
+                                         per_head, causal, wl, wr, float(np.float32(scale)))
+    assert_close(o, lse, o_ref, lse_ref, str(case))
+    ref = oracle.skip_map_ex(bits, per_head, B, Hq, Sq, Sk, causal, wl, wr, 128, 128)
+    ref = ref.reshape(B, -1, ref.shape[1], ref.shape[2])
+    if ref.shape[1] == 1:
+        ref = np.repeat(ref, Hq, axis=1)
+    assert np.array_equal(vis, ref)
+
+
+def test_ex_defaults_are_attn_fwd():
+    B, Hq, Hkv, S, d = 2, 4, 2, 333, 128
+    q, k, v = inp.qkv(B, Hq, Hkv, S, d, inp.BF16, 1)
+    bits = inp.pack_bits(inp.bernoulli_mask(B, S, 1))
+    for causal in (False, True):
+        for b in (None, bits):
+            a = _run(q, k, v, b, False, causal, -1, -1, 0.1)
+            qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+            o = torch.empty_like(qd)
+            lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+            md = None if b is None else torch.from_numpy(b.view(np.int32)).cuda()
+            af.attn_fwd(qd, kd, vd, o, lse, md, causal=causal, scale=0.1)
+            af.attn_check()
+            assert np.array_equal(a[0], o.float().cpu().numpy()) and np.array_equal(a[1], lse.cpu().numpy())
