@@ -59,9 +59,10 @@ constexpr int O_COL0 = 256;    // O_t (fp32, d columns) at 256 + t*128
 constexpr int FLAG_END = 4;    // info entry marking the end of a work unit
 constexpr float LN2 = 0.69314718055994530942f;
 
-// NONE: every key; BAND: keys in [key_lo(i), key_hi(i)) per query row (causal, sliding
-// windows); CUSTOM: kept-bit words from the mask pre-pass (which folds the band in).
-enum MaskMode { MASK_NONE = 0, MASK_BAND = 1, MASK_CUSTOM = 2 };
+// NONE: every key; CAUSAL: keys up to the aligned position; BAND: keys in
+// [key_lo(i), key_hi(i)) per query row (sliding windows); CUSTOM: kept-bit words from the
+// mask pre-pass (which folds any band in).  The first two keep their bounds cheap.
+enum MaskMode { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_CUSTOM = 2, MASK_BAND = 3 };
 
 template <int D, int MODE>
 struct Layout {
@@ -225,7 +226,7 @@ template <int D, bool BF16, int MODE>
 __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_t* gbase,
                                           volatile int* abort_flag, int lane) {
   using L = Layout<D, MODE>;
-  const bool causal = p.causal != 0;
+  const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -398,7 +399,7 @@ template <int D, bool BF16, int MODE>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t* gbase,
                                          volatile int* abort_flag, uint32_t tmem, int lane) {
   using L = Layout<D, MODE>;
-  const bool causal = p.causal != 0;
+  const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -516,7 +517,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
                                              int quarter, int lane) {
   using L = Layout<D, MODE>;
   using OutT = uint16_t;
-  const bool causal = p.causal != 0;
+  const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
   const unsigned long long to = p.timeout_ns;
   const uint32_t bars = base + L::OFF_BAR;
   const uint32_t* words = reinterpret_cast<const uint32_t*>(gbase + L::OFF_WORDS);
@@ -566,8 +567,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
 
       // Mask: excluded scores become -inf (weight exactly 0).
       // band / key bound: kept columns of this tile are [lo, hi) relative to its first key
-      const int hi = (MODE == MASK_NONE ? p.Sk : key_hi(p, i)) - j * BN;
-      const int lo = (MODE == MASK_NONE ? 0 : key_lo(p, i)) - j * BN;
+      const int hi = (MODE == MASK_NONE ? p.Sk
+                      : MODE == MASK_CAUSAL ? min(p.Sk, i + p.off + 1)
+                                            : key_hi(p, i)) - j * BN;
+      const int lo = (MODE == MASK_BAND) ? key_lo(p, i) - j * BN : 0;
       const bool edge = (MODE != MASK_CUSTOM) && __any_sync(0xffffffffu, hi < BN || lo > 0);
       const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
       auto mask_half = [&](uint32_t(&h)[64], int c0) {
@@ -951,6 +954,7 @@ template <int D, bool BF16>
 int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev) {
   switch (mode) {
     case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st, dev);
+    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st, dev);
     case MASK_BAND: return launch<D, BF16, MASK_BAND>(p, grid, st, dev);
     default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st, dev);
   }
@@ -1029,7 +1033,10 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   p.timeout_ns = g_timeout_ns.load();
   p.inject = g_inject.exchange(0);
   const int grid = p.num_units < sms ? p.num_units : sms;
-  const int mode = a.mask_bits ? MASK_CUSTOM : ((p.wl >= 0 || p.er >= 0) ? MASK_BAND : MASK_NONE);
+  const int mode = a.mask_bits                        ? MASK_CUSTOM
+                   : (p.wl < 0 && p.er < 0)            ? MASK_NONE
+                   : (p.wl < 0 && p.er == 0)           ? MASK_CAUSAL
+                                                       : MASK_BAND;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(a.stream);
   // Custom masks: stream-ordered scratch for the pre-pass output, freed in stream order
   // after the launch that reads it.
