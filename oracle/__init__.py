@@ -61,9 +61,9 @@ def _load():
             lib.oracle_attn_fwd.restype = i
             lib.oracle_skip_map.argtypes = [p, i, i, i, i, i, p]
             lib.oracle_skip_map.restype = i
-            lib.oracle_attn_rows_ex.argtypes = [p, p, p, i, p, i, i, i, i, i, i, i, i, i, i, d, p, i64, p, p, i]
+            lib.oracle_attn_rows_ex.argtypes = [p, p, p, i, p, i, i, i, i, i, i, i, i, i, i, p, p, d, p, i64, p, p, i]
             lib.oracle_attn_rows_ex.restype = i
-            lib.oracle_skip_map_ex.argtypes = [p, i, i, i, i, i, i, i, i, i, i, p]
+            lib.oracle_skip_map_ex.argtypes = [p, i, i, i, i, i, i, i, i, p, p, i, i, p]
             lib.oracle_skip_map_ex.restype = i
             lib.oracle_widen.argtypes = [ctypes.c_uint16, i]
             lib.oracle_widen.restype = d
@@ -135,11 +135,16 @@ def skip_map(mask_bits, B, S, causal, bm, bn):
     return out
 
 
+def _lens(x):
+    return None if x is None else np.ascontiguousarray(x, dtype=np.int32)
+
+
 def attn_rows_ex(q, k, v, dtype, rows=None, mask_bits=None, mask_per_head=False, causal=False,
-                 window_left=-1, window_right=-1, scale=None, nthreads=0):
+                 window_left=-1, window_right=-1, scale=None, nthreads=0, seqlens_q=None, seqlens_k=None):
     """Extended definition (see attn_oracle.c): q [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] with Sq <= Sk,
     bottom-right aligned; optional key band; masks [B,Sq,W] or per head [B,Hq,Sq,W].
-    rows=None evaluates every row and returns O [B,Hq,Sq,d], LSE [B,Hq,Sq]."""
+    rows=None evaluates every row and returns O [B,Hq,Sq,d], LSE [B,Hq,Sq].  seqlens_q / seqlens_k
+    (int [B]) give each batch entry its own lengths; rows past them come back as NaN."""
     for name, a in (("q", q), ("k", k), ("v", v)):
         if a.dtype != np.uint16 or a.ndim != 4 or not a.flags.c_contiguous:
             raise ValueError(f"{name} must be a C-contiguous uint16 [B,H,S,d] array")
@@ -159,9 +164,11 @@ def attn_rows_ex(q, k, v, dtype, rows=None, mask_bits=None, mask_per_head=False,
     n = rows.shape[0]
     o = np.empty((n, d), np.float64)
     lse = np.empty((n,), np.float64)
+    lq, lk = _lens(seqlens_q), _lens(seqlens_k)
     rc = _load().oracle_attn_rows_ex(_ptr(q), _ptr(k), _ptr(v), int(dtype), _ptr(mask_bits), int(bool(mask_per_head)),
                                      B, Hq, Hkv, Sq, Sk, d, int(bool(causal)), int(window_left), int(window_right),
-                                     float(scale), _ptr(rows), n, _ptr(o), _ptr(lse), int(nthreads))
+                                     _ptr(lq), _ptr(lk), float(scale), _ptr(rows), n, _ptr(o), _ptr(lse),
+                                     int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows_ex failed ({rc})")
     if full:
@@ -169,14 +176,16 @@ def attn_rows_ex(q, k, v, dtype, rows=None, mask_bits=None, mask_per_head=False,
     return o, lse
 
 
-def skip_map_ex(mask_bits, mask_per_head, B, Hq, Sq, Sk, causal, window_left, window_right, bm, bn):
+def skip_map_ex(mask_bits, mask_per_head, B, Hq, Sq, Sk, causal, window_left, window_right, bm, bn,
+                seqlens_q=None, seqlens_k=None):
     """uint8 [B*Hm, ceil(Sq/bm), ceil(Sk/bn)], Hm = Hq for per-head masks else 1."""
     if mask_bits is not None:
         mask_bits = np.ascontiguousarray(mask_bits, dtype=np.uint32)
     Hm = Hq if (mask_bits is not None and mask_per_head) else 1
     out = np.zeros((B * Hm, (Sq + bm - 1) // bm, (Sk + bn - 1) // bn), np.uint8)
+    lq, lk = _lens(seqlens_q), _lens(seqlens_k)
     rc = _load().oracle_skip_map_ex(_ptr(mask_bits), int(bool(mask_per_head)), B, Hq, Sq, Sk, int(bool(causal)),
-                                    int(window_left), int(window_right), bm, bn, _ptr(out))
+                                    int(window_left), int(window_right), _ptr(lq), _ptr(lk), bm, bn, _ptr(out))
     if rc != 0:
         raise RuntimeError(f"oracle_skip_map_ex failed ({rc})")
     return out

@@ -258,13 +258,17 @@ int oracle_skip_map(const uint32_t *mask_bits, int B, int S, int causal, int bm,
  * oracle_attn_rows_ex: the extended definition.  q, o: [B][Hq][Sq][d]; k, v:
  * [B][Hkv][Sk][d]; mask_bits: [B][Sq][ceil(Sk/32)] (mask_per_head = 0) or
  * [B][Hq][Sq][ceil(Sk/32)] (mask_per_head = 1) or NULL; rows are flat ids
- * (b*Hq + hq)*Sq + i.  Same outputs as oracle_attn_rows.
+ * (b*Hq + hq)*Sq + i.  Same outputs as oracle_attn_rows.  seqlens_q / seqlens_k (NULL =
+ * all Sq / Sk) give batch entry b its own lengths sq_b <= Sq and sk_b <= Sk inside the
+ * padded buffers: its query i sits at key position i + sk_b - sq_b, only keys j < sk_b
+ * exist, and rows i >= sq_b have no value (written as NaN).
  */
 int oracle_attn_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                         const uint32_t *mask_bits, int mask_per_head, int B, int Hq, int Hkv,
                         int Sq, int Sk, int d, int causal, int window_left, int window_right,
-                        double scale, const int64_t *rows, int64_t nrows, double *o_out,
-                        double *lse_out, int nthreads)
+                        const int *seqlens_q, const int *seqlens_k, double scale,
+                        const int64_t *rows, int64_t nrows, double *o_out, double *lse_out,
+                        int nthreads)
 {
     if (!q || !k || !v || !rows || !o_out || !lse_out)
         return -1;
@@ -273,6 +277,10 @@ int oracle_attn_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     int64_t total = (int64_t)B * Hq * Sq;
     for (int64_t r = 0; r < nrows; r++)
         if (rows[r] < 0 || rows[r] >= total)
+            return -1;
+    for (int b = 0; b < B; b++)
+        if ((seqlens_q && (seqlens_q[b] < 0 || seqlens_q[b] > Sq)) ||
+            (seqlens_k && (seqlens_k[b] < 0 || seqlens_k[b] > Sk)))
             return -1;
 #ifdef _OPENMP
     if (nthreads > 0)
@@ -295,7 +303,15 @@ int oracle_attn_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 const int64_t row_id = rows[r];
                 const int64_t i = row_id % Sq, bh = row_id / Sq, hq = bh % Hq, b = bh / Hq;
                 const int64_t hkv = hq / (Hq / Hkv);
-                const int64_t pos = i + Sk - Sq;
+                const int64_t sq_b = seqlens_q ? seqlens_q[b] : Sq;
+                const int64_t sk_b = seqlens_k ? seqlens_k[b] : Sk;
+                if (i >= sq_b) {
+                    for (int t = 0; t < d; t++)
+                        o_out[r * d + t] = NAN;
+                    lse_out[r] = NAN;
+                    continue;
+                }
+                const int64_t pos = i + sk_b - sq_b;
                 const uint16_t *qi = q + ((b * Hq + hq) * Sq + i) * d;
                 const uint16_t *kb = k + (b * Hkv + hkv) * (int64_t)Sk * d;
                 const uint16_t *vb = v + (b * Hkv + hkv) * (int64_t)Sk * d;
@@ -306,7 +322,8 @@ int oracle_attn_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 double m = -INFINITY;
                 int any = 0;
                 for (int64_t j = 0; j < Sk; j++) {
-                    keep[j] = (unsigned char)allowed_ex(mrow, pos, j, causal, window_left, window_right);
+                    keep[j] = (unsigned char)(j < sk_b &&
+                                              allowed_ex(mrow, pos, j, causal, window_left, window_right));
                     if (!keep[j])
                         continue;
                     double dot = 0.0;
@@ -345,31 +362,36 @@ int oracle_attn_rows_ex(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
 /*
  * oracle_skip_map_ex: block emptiness under the extended rule, out [B*Hm][nqt][nkt] with
- * Hm = Hq if mask_per_head else 1, nqt = ceil(Sq/bm), nkt = ceil(Sk/bn).
+ * Hm = Hq if mask_per_head else 1, nqt = ceil(Sq/bm), nkt = ceil(Sk/bn); per-entry lengths
+ * as for oracle_attn_rows_ex.
  */
 int oracle_skip_map_ex(const uint32_t *mask_bits, int mask_per_head, int B, int Hq, int Sq, int Sk,
-                       int causal, int window_left, int window_right, int bm, int bn,
-                       unsigned char *out)
+                       int causal, int window_left, int window_right, const int *seqlens_q,
+                       const int *seqlens_k, int bm, int bn, unsigned char *out)
 {
     if (!out || B < 1 || Sq < 1 || Sk < Sq || bm < 1 || bn < 1)
         return -1;
     const int nqt = (Sq + bm - 1) / bm, nkt = (Sk + bn - 1) / bn;
     const int Hm = (mask_bits && mask_per_head) ? Hq : 1;
     const int64_t W = (Sk + 31) / 32;
-    for (int64_t bh = 0; bh < (int64_t)B * Hm; bh++)
+    for (int64_t bh = 0; bh < (int64_t)B * Hm; bh++) {
+        const int64_t b = bh / Hm;
+        const int64_t sq_b = seqlens_q ? seqlens_q[b] : Sq;
+        const int64_t sk_b = seqlens_k ? seqlens_k[b] : Sk;
         for (int qt = 0; qt < nqt; qt++)
             for (int kt = 0; kt < nkt; kt++) {
                 int hit = 0;
-                for (int64_t i = (int64_t)qt * bm; i < Sq && i < (int64_t)(qt + 1) * bm && !hit; i++) {
+                for (int64_t i = (int64_t)qt * bm; i < sq_b && i < (int64_t)(qt + 1) * bm && !hit; i++) {
                     const uint32_t *mrow = mask_bits ? mask_bits + (bh * Sq + i) * W : NULL;
-                    for (int64_t j = (int64_t)kt * bn; j < Sk && j < (int64_t)(kt + 1) * bn; j++)
-                        if (allowed_ex(mrow, i + Sk - Sq, j, causal, window_left, window_right)) {
+                    for (int64_t j = (int64_t)kt * bn; j < sk_b && j < (int64_t)(kt + 1) * bn; j++)
+                        if (allowed_ex(mrow, i + sk_b - sq_b, j, causal, window_left, window_right)) {
                             hit = 1;
                             break;
                         }
                 }
                 out[(bh * nqt + qt) * nkt + kt] = (unsigned char)hit;
             }
+    }
     return 0;
 }
 

@@ -120,3 +120,46 @@ def test_extended_matches_torch_sdpa():
     np.testing.assert_allclose(o[ok], ref[ok], rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(lse[ok], lref[ok], rtol=1e-12, atol=1e-12)
     assert np.all(o[~ok] == 0) and np.all(np.isneginf(lse[~ok]))
+
+
+def test_varlen_entries_equal_separate_problems():
+    """Each batch entry with its own lengths equals the same entry run alone at those lengths
+    (which the pins above tie to the base definition); padded rows have no value."""
+    B, Hq, Hkv, Sq, Sk, d = 3, 2, 1, 40, 70, 8
+    q, k, v = inp.qkv(B, Hq, Hkv, Sk, d, inp.BF16, 12)
+    q = q[:, :, :Sq].contiguous()
+    lq = np.array([40, 17, 0], np.int32)
+    lk = np.array([70, 25, 9], np.int32)
+    keep = inp.bernoulli_mask(B, Sk, 12)[:, :Sq]
+    bits = inp.pack_bits(keep)
+    for causal, wl, wr, mb in ((True, -1, -1, None), (False, 6, 2, bits), (True, 11, -1, bits)):
+        o, lse = oracle.attn_rows_ex(_u16(q), _u16(k), _u16(v), inp.BF16, None, mb, False, causal, wl, wr, 0.3,
+                                     seqlens_q=lq, seqlens_k=lk)
+        for b in range(B):
+            sq, sk = int(lq[b]), int(lk[b])
+            assert np.all(np.isnan(lse[b, :, sq:])) and np.all(np.isnan(o[b, :, sq:]))
+            if sq == 0:
+                continue
+            qb = q[b:b + 1, :, :sq].contiguous()
+            kb, vb = k[b:b + 1, :, :sk].contiguous(), v[b:b + 1, :, :sk].contiguous()
+            mbb = None if mb is None else inp.pack_bits(keep[b:b + 1, :sq, :sk])
+            if sk >= sq:
+                ref = oracle.attn_rows_ex(_u16(qb), _u16(kb), _u16(vb), inp.BF16, None, mbb, False, causal, wl, wr, 0.3)
+                assert np.array_equal(o[b:b + 1, :, :sq], ref[0]) and np.array_equal(lse[b:b + 1, :, :sq], ref[1])
+        # the skip map agrees with the rows that have a kept entry
+        m = oracle.skip_map_ex(mb, False, B, Hq, Sq, Sk, causal, wl, wr, 16, 16, seqlens_q=lq, seqlens_k=lk)
+        assert m.shape == (B, 3, 5)
+        assert not m[2].any()  # entry 2 has no query rows
+
+
+def test_varlen_short_keys_make_early_rows_empty_under_causal():
+    """sk_b < sq_b: query i sits at key position i + sk_b - sq_b < 0 for the first rows, so
+    under causal they keep nothing (O = 0, LSE = -inf); later rows match the tail problem."""
+    B, H, Sq, Sk, d = 1, 1, 12, 12, 4
+    q, k, v = inp.qkv(B, H, H, Sk, d, inp.F16, 13)
+    o, lse = oracle.attn_rows_ex(_u16(q), _u16(k), _u16(v), inp.F16, None, None, False, True, -1, -1, 0.5,
+                                 seqlens_q=np.array([10], np.int32), seqlens_k=np.array([6], np.int32))
+    assert np.all(np.isneginf(lse[0, 0, :4])) and np.all(o[0, 0, :4] == 0)
+    tail = oracle.attn_rows_ex(_u16(q[:, :, 4:10].contiguous()), _u16(k[:, :, :6].contiguous()),
+                               _u16(v[:, :, :6].contiguous()), inp.F16, None, None, False, True, -1, -1, 0.5)
+    assert np.array_equal(o[:, :, 4:10], tail[0]) and np.array_equal(lse[:, :, 4:10], tail[1])
