@@ -42,7 +42,8 @@ class FwdParams(ctypes.Structure):
                 ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Sq", ctypes.c_int),
                 ("Sk", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int), ("window_left", ctypes.c_int),
                 ("window_right", ctypes.c_int), ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
-                ("stream", ctypes.c_void_p), ("visited", ctypes.c_void_p)]
+                ("stream", ctypes.c_void_p), ("visited", ctypes.c_void_p), ("seqlens_q", ctypes.c_void_p),
+                ("seqlens_k", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -106,6 +107,13 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; fp16 or bf16 expected")
 
 
+def _lens_ptr(t, B):
+    import torch
+    if t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous():
+        raise ValueError("sequence lengths must be a contiguous int32 tensor of B entries")
+    return t.data_ptr()
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -156,10 +164,11 @@ def attn_fwd_noalloc(q, k, v, o, lse=None, mask_bits=None, causal=False, scale=N
 
 
 def attn_fwd_ex(q, k, v, o, lse=None, mask_bits=None, mask_per_head=False, causal=False, window_left=-1,
-                window_right=-1, scale=None, visited=None, stream=None):
+                window_right=-1, scale=None, visited=None, stream=None, seqlens_q=None, seqlens_k=None):
     """Generalised forward: q/o [B,Hq,Sq,d], k/v [B,Hkv,Sk,d] with Sk >= Sq (bottom-right
     aligned), a band of kept keys (window_left / window_right, -1 = unbounded), custom masks
-    [B,Sq,ceil(Sk/32)] or per head [B,Hq,Sq,ceil(Sk/32)]; see include/attn.h."""
+    [B,Sq,ceil(Sk/32)] or per head [B,Hq,Sq,ceil(Sk/32)], per-entry lengths seqlens_q /
+    seqlens_k (int32 device tensors [B]); see include/attn.h."""
     B, Hq, Sq, d = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     if scale is None:
@@ -170,7 +179,9 @@ def attn_fwd_ex(q, k, v, o, lse=None, mask_bits=None, mask_per_head=False, causa
                     mask_per_head=int(bool(mask_per_head)), B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d,
                     causal=int(bool(causal)), window_left=int(window_left), window_right=int(window_right),
                     scale=float(scale), dtype=_dtype_code(q), stream=_stream_handle(stream).value,
-                    visited=None if visited is None else visited.data_ptr())
+                    visited=None if visited is None else visited.data_ptr(),
+                    seqlens_q=None if seqlens_q is None else _lens_ptr(seqlens_q, B),
+                    seqlens_k=None if seqlens_k is None else _lens_ptr(seqlens_k, B))
     rc = library().attn_fwd_ex(ctypes.byref(prm))
     if rc != 0:
         raise AttnError(rc, "attn_fwd_ex")

@@ -104,7 +104,7 @@ struct Layout {
 struct InfoHdr {
   int j;      // key tile index
   int flags;  // bit t: Q tile t computes this key tile; FLAG_END: end of unit
-  int pad[2];
+  int sq, sk;  // the unit's query and key lengths (per batch entry with seqlens arrays)
 };
 
 struct Params {
@@ -115,10 +115,13 @@ struct Params {
   const uint8_t* tflags;  // [B][nqt][nkt] 1 = block holds a kept entry (custom masks)
   uint8_t* visited;
   int B, Hq, Hkv, Sq, Sk, g, nqb, nkt, nqt, W, num_units;
-  // Query row i sits at key position i + off (off = Sk - Sq, bottom-right alignment); the
-  // band keeps keys with pos - wl <= key <= pos + er (wl / er = -1: unbounded).
-  int off, wl, er;
+  // Query row i of a batch entry with sq queries and sk keys sits at key position
+  // i + off, off = sk - sq (bottom-right alignment); the band keeps keys with
+  // pos - wl <= key <= pos + er (wl / er = -1: unbounded).
+  int wl, er;
   int mask_heads;  // custom-mask rows per batch entry: Hq (per-head masks) or 1
+  const int* lens_q;  // per batch entry query / key lengths inside the padded buffers,
+  const int* lens_k;  // clamped to [0, Sq] / [0, Sk]; NULL = Sq / Sk
   int causal;      // the band only bounds keys on the right: longest units first
   int inject;
   float scale_log2;
@@ -198,12 +201,18 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
   }
 }
 
-// Kept keys of query row i under the band: [key_lo, key_hi).
-__device__ __forceinline__ int key_lo(const Params& p, int i) {
-  return p.wl < 0 ? 0 : max(0, i + p.off - p.wl);
+// Query / key lengths of batch entry b (off = sk - sq is its bottom-right alignment).
+__device__ __forceinline__ void unit_lengths(const Params& p, int b, int& sq, int& sk) {
+  sq = p.lens_q ? min(max(__ldg(p.lens_q + b), 0), p.Sq) : p.Sq;
+  sk = p.lens_k ? min(max(__ldg(p.lens_k + b), 0), p.Sk) : p.Sk;
 }
-__device__ __forceinline__ int key_hi(const Params& p, int i) {
-  return p.er < 0 ? p.Sk : min(p.Sk, i + p.off + p.er + 1);
+
+// Kept keys of query row i under the band: [key_lo, key_hi) (empty when hi <= lo).
+__device__ __forceinline__ int key_lo(const Params& p, int i, int off) {
+  return p.wl < 0 ? 0 : max(0, i + off - p.wl);
+}
+__device__ __forceinline__ int key_hi(const Params& p, int i, int off, int sk) {
+  return p.er < 0 ? sk : min(sk, i + off + p.er + 1);
 }
 
 }  // namespace attn
@@ -273,16 +282,24 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     }
     inject = false;
 
-    // Key-tile range of each Q tile under the band (key_lo / key_hi grow with the row).
+    int sq, sk;
+    unit_lengths(p, b, sq, sk);
+    const int off = sk - sq;
+    // Key-tile range of each Q tile under the band.  key_lo / key_hi grow by one per row,
+    // so the kept keys of rows rf..r1 form the one range [key_lo(rf), key_hi(r1)), rf being
+    // the first row whose band is not empty (rows at key position < -er keep nothing).
     int jlo[QT], jhi[QT];
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
       const int r0 = row0 + t * BM;
-      const int r1 = min(r0 + BM - 1, p.Sq - 1);
-      jlo[t] = key_lo(p, r0) / BN;
-      jhi[t] = r0 < p.Sq ? (key_hi(p, r1) - 1) / BN : -1;  // -1: no such Q tile
+      const int r1 = min(r0 + BM - 1, sq - 1);
+      const int rf = p.er >= 0 ? max(r0, -off - p.er) : r0;
+      const int klo = key_lo(p, rf, off), khi = key_hi(p, r1, off, sk);
+      const bool any = r0 < sq && rf <= r1 && khi > klo;
+      jlo[t] = any ? klo / BN : 0;
+      jhi[t] = any ? (khi - 1) / BN : -1;  // -1: nothing to compute for this Q tile
     }
-    const int jbeg = (jhi[1] >= 0) ? min(jlo[0], jlo[1]) : jlo[0];
+    const int jbeg = jhi[0] < 0 ? jlo[1] : (jhi[1] < 0 ? jlo[0] : min(jlo[0], jlo[1]));
     const int jend = max(jhi[0], jhi[1]) + 1;
     const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
     uint32_t f0 = 0, f1 = 0;  // bit (j % 32): Q tile 0 / 1 has a kept entry in key tile j
@@ -312,6 +329,8 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       if (lane == 0) {
         hdr[ie].j = j;
         hdr[ie].flags = (a0 ? 1 : 0) | (a1 ? 2 : 0);
+        hdr[ie].sq = sq;
+        hdr[ie].sk = sk;
         const uint32_t fb = bars + 8u * (L::B_IFULL + ie);
         if constexpr (MODE == MASK_CUSTOM) {
           // the block's kept-bit words (256 rows x 4 words) land in the descriptor slot
@@ -361,6 +380,8 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     if (lane == 0) {
       hdr[ie].j = -1;
       hdr[ie].flags = FLAG_END;
+      hdr[ie].sq = sq;
+      hdr[ie].sk = sk;
       mbar_arrive(bars + 8u * (L::B_IFULL + ie));
     }
     __syncwarp();
@@ -539,11 +560,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     const int i = qb * UNIT_ROWS + t * BM + r;
     float m = -INFINITY, l = 0.f;
     int nact = 0;
+    int sq = p.Sq, sk = p.Sk;  // the unit's lengths, carried by every tile descriptor
 
     while (true) {
       if (!bwait_warp(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) return;
       const int j = hdr[ie].j;
       const int flags = hdr[ie].flags;
+      sq = hdr[ie].sq;
+      sk = hdr[ie].sk;
       const bool end = (flags & FLAG_END) != 0;
       const bool act = !end && ((flags >> t) & 1);
       uint4 wv = make_uint4(0u, 0u, 0u, 0u);
@@ -567,10 +591,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
 
       // Mask: excluded scores become -inf (weight exactly 0).
       // band / key bound: kept columns of this tile are [lo, hi) relative to its first key
-      const int hi = (MODE == MASK_NONE ? p.Sk
-                      : MODE == MASK_CAUSAL ? min(p.Sk, i + p.off + 1)
-                                            : key_hi(p, i)) - j * BN;
-      const int lo = (MODE == MASK_BAND) ? key_lo(p, i) - j * BN : 0;
+      const int off = sk - sq;
+      const int hi = (MODE == MASK_NONE ? sk
+                      : MODE == MASK_CAUSAL ? min(sk, i + off + 1)
+                                            : key_hi(p, i, off, sk)) - j * BN;
+      const int lo = (MODE == MASK_BAND) ? key_lo(p, i, off) - j * BN : 0;
       const bool edge = (MODE != MASK_CUSTOM) && __any_sync(0xffffffffu, hi < BN || lo > 0);
       const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
       auto mask_half = [&](uint32_t(&h)[64], int c0) {
@@ -671,7 +696,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       o_par ^= 1u;
       tc_fence_after();
     }
-    const bool row_ok = i < p.Sq;
+    const bool row_ok = i < sq;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + (row_ok ? i : 0)) * D;
 #pragma unroll
@@ -803,6 +828,9 @@ __global__ void __launch_bounds__(256) mask_prepass_kernel(const uint32_t* __res
   const int qt = (int)(rest % p.nqt);
   const long long mbk = rest / p.nqt;
   const int W4 = 4 * p.nkt;
+  int sq, sk;
+  unit_lengths(p, (int)(mbk / p.mask_heads), sq, sk);
+  const int off = sk - sq;
   uint32_t any = 0;
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
@@ -810,7 +838,9 @@ __global__ void __launch_bounds__(256) mask_prepass_kernel(const uint32_t* __res
     if (i >= p.Sq) continue;
     const uint32_t* src = mask + ((size_t)mbk * p.Sq + i) * p.W;
     uint32_t* dst = words4 + ((size_t)mbk * p.Sq + i) * W4;
-    const int klo = key_lo(p, i), khi = key_hi(p, i);  // khi <= Sk
+    // rows past the entry's length keep nothing; keys past it do not exist
+    const int klo = key_lo(p, i, off);
+    const int khi = i < sq ? key_hi(p, i, off, sk) : 0;  // <= sk
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const int gw = kt * 4 + w;
@@ -995,7 +1025,9 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   if (!(a.scale > 0.f) || !std::isfinite(a.scale)) return ATTN_ERR_INVALID;
   const uintptr_t a16 = (uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o;
   if (a16 & 15u) return ATTN_ERR_INVALID;
-  if (((uintptr_t)a.lse & 3u) || ((uintptr_t)a.mask_bits & 3u)) return ATTN_ERR_INVALID;
+  if (((uintptr_t)a.lse & 3u) || ((uintptr_t)a.mask_bits & 3u) || ((uintptr_t)a.seqlens_q & 3u) ||
+      ((uintptr_t)a.seqlens_k & 3u))
+    return ATTN_ERR_INVALID;
   const long long nqb = (a.Sq + UNIT_ROWS - 1) / UNIT_ROWS;
   if ((long long)a.B * a.Hq * a.Sk > INT_MAX || (long long)a.B * a.Hq * nqb > INT_MAX)
     return ATTN_ERR_INVALID;
@@ -1024,10 +1056,11 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   p.nqt = (a.Sq + BM - 1) / BM;
   p.W = (a.Sk + 31) / 32;
   p.num_units = a.B * a.Hq * (int)nqb;
-  p.off = a.Sk - a.Sq;
   p.wl = a.window_left;
   p.er = a.causal ? 0 : a.window_right;  // causal: nothing right of the aligned position
   p.mask_heads = (a.mask_bits && a.mask_per_head) ? a.Hq : 1;
+  p.lens_q = a.seqlens_q;
+  p.lens_k = a.seqlens_k;
   p.causal = (p.er >= 0 && p.wl < 0) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.timeout_ns = g_timeout_ns.load();

@@ -88,7 +88,14 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *   - custom masks of [B][Sq][ceil(Sk/32)] words (mask_per_head = 0) or
  *     [B][Hq][Sq][ceil(Sk/32)] (mask_per_head = 1), ANDed with the band.
  *   - visited: as for attn_fwd_visited (nqt = ceil(Sq/bm), nkt = ceil(Sk/bn)), or NULL.
- * With Sq = Sk = S, windows -1 and mask_per_head = 0 it is attn_fwd.  Custom masks take
+ *   - variable-length batches: seqlens_q / seqlens_k, int32 [B] in device memory (4-byte
+ *     aligned) or NULL (= Sq / Sk for every entry), give batch entry b its own lengths
+ *     sq_b <= Sq and sk_b <= Sk inside the padded buffers above (values outside [0, Sq] /
+ *     [0, Sk] are clamped).  Entry b's query i sits at key position i + sk_b - sq_b, only
+ *     keys j < sk_b exist, and rows i >= sq_b of o and lse are not written.  Key rows at or
+ *     past sk_b get weight exactly 0, so v must hold finite values there (0 * inf is NaN);
+ *     k there may hold anything.  The custom-mask layout keeps the padded shape.
+ * With Sq = Sk = S, windows -1, mask_per_head = 0 and no lengths it is attn_fwd.  Custom masks take
  * stream-ordered scratch of nm*Sq*ceil(Sk/128)*16 + nm*ceil(Sq/128)*ceil(Sk/128) bytes,
  * nm = B (or B*Hq per head).  Errors as for attn_fwd; Sk < Sq is ATTN_ERR_INVALID.
  */
@@ -104,6 +111,7 @@ typedef struct {
     int dtype;
     void *stream;
     uint8_t *visited;
+    const int *seqlens_q, *seqlens_k;
 } attn_fwd_params_t;
 
 int attn_fwd_ex(const attn_fwd_params_t *params);

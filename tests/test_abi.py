@@ -103,6 +103,7 @@ def test_fwd_ex_validation(lib):
     base = dict(q=P, k=P, v=P, o=P, B=1, Hq=2, Hkv=2, Sq=128, Sk=256, d=64, causal=1, window_left=-1,
                 window_right=-1, scale=0.125, dtype=0)
     for kw, status in ((dict(Sk=64), -1), (dict(window_left=-2), -1), (dict(window_right=-5), -1),
-                       (dict(mask_per_head=2), -1), (dict(d=80), -2), (dict(Sq=0), -1)):
+                       (dict(mask_per_head=2), -1), (dict(d=80), -2), (dict(Sq=0), -1),
+                       (dict(seqlens_q=P + 2), -1), (dict(seqlens_k=P + 1), -1)):
         args = dict(base, **kw)
         assert lib.attn_fwd_ex(ctypes.byref(FwdParams(**args))) == status, kw

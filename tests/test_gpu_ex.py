@@ -80,3 +80,90 @@ def test_ex_defaults_are_attn_fwd():
             af.attn_fwd(qd, kd, vd, o, lse, md, causal=causal, scale=0.1)
             af.attn_check()
             assert np.array_equal(a[0], o.float().cpu().numpy()) and np.array_equal(a[1], lse.cpu().numpy())
+
+
+VARLEN_CASES = [
+    # B, Hq, Hkv, Sq, Sk, d, dtype, causal, wl, wr, mask
+    (4, 2, 1, 300, 300, 128, inp.BF16, True, -1, -1, None),
+    (4, 4, 2, 257, 520, 64, inp.F16, False, -1, -1, None),
+    (3, 2, 2, 384, 700, 128, inp.F16, False, 90, 20, None),
+    (4, 2, 1, 260, 400, 64, inp.BF16, True, -1, -1, "shared"),
+    (3, 4, 4, 200, 333, 128, inp.BF16, True, 64, -1, "head"),
+]
+
+
+def _lengths(B, Sq, Sk, seed):
+    """Per-entry lengths with the edge cases in the first entries: an entry with no queries,
+    one with fewer keys than queries, one at the full padded size; the rest random."""
+    g = np.random.default_rng(seed)
+    lq = g.integers(1, Sq + 1, size=B).astype(np.int32)
+    lk = g.integers(1, Sk + 1, size=B).astype(np.int32)
+    lq[0], lk[0] = 0, Sk // 2
+    if B > 1:
+        lq[1], lk[1] = Sq, max(1, Sq // 3)
+    if B > 2:
+        lq[2], lk[2] = Sq, Sk
+    return lq, lk
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=lambda c: "B{}_Hq{}_Sq{}_Sk{}_d{}_c{}_w{}_{}_{}".format(
+    c[0], c[1], c[3], c[4], c[5], int(c[7]), c[8], c[9], c[10]))
+def test_varlen_parity_and_skip_map(case):
+    """Per-entry lengths inside padded buffers: rows below sq_b match the oracle (bottom-right
+    alignment per entry), rows at or past it are left untouched, key rows past sk_b do not
+    reach the result even when k holds NaN there, and the skip map is exact."""
+    B, Hq, Hkv, Sq, Sk, d, dtype, causal, wl, wr, mask = case
+    q, k, v = inp.qkv(B, Hq, Hkv, Sk, d, dtype, 7 * Sq + Sk)
+    q = q[:, :, :Sq].contiguous()
+    lq, lk = _lengths(B, Sq, Sk, Sq + Sk)
+    per_head = mask == "head"
+    bits = None
+    if mask == "shared":
+        bits = inp.pack_bits(inp.bernoulli_mask(B, Sk, 5)[:, :Sq])
+    elif mask == "head":
+        bits = inp.pack_bits(inp.bernoulli_mask(B * Hq, Sk, 6)[:, :Sq]).reshape(B, Hq, Sq, -1)
+    k_nan = k.clone()
+    for b in range(B):
+        k_nan[b, :, int(lk[b]):] = float("nan")
+    dev = "cuda"
+    qd, kd, vd = q.to(dev), k_nan.to(dev), v.to(dev)
+    md = None if bits is None else torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device=dev)
+    vis = torch.zeros((B, Hq, -(-Sq // 128), -(-Sk // 128)), dtype=torch.uint8, device=dev)
+    scale = 1.0 / d ** 0.5
+    af.attn_fwd_ex(qd, kd, vd, o, lse, md, per_head, causal, wl, wr, scale, vis,
+                   seqlens_q=torch.from_numpy(lq).to(dev), seqlens_k=torch.from_numpy(lk).to(dev))
+    af.attn_check()
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    o_ref, lse_ref = oracle.attn_rows_ex(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), dtype, None, bits, per_head,
+                                         causal, wl, wr, float(np.float32(scale)), seqlens_q=lq, seqlens_k=lk)
+    for b in range(B):
+        n = int(lq[b])
+        assert np.all(np.isnan(o[b, :, n:])) and np.all(np.isnan(lse[b, :, n:])), f"entry {b}: padded rows written"
+        if n:
+            assert_close(o[b, :, :n], lse[b, :, :n], o_ref[b, :, :n], lse_ref[b, :, :n], f"{case} entry {b}")
+    ref = oracle.skip_map_ex(bits, per_head, B, Hq, Sq, Sk, causal, wl, wr, 128, 128, seqlens_q=lq, seqlens_k=lk)
+    ref = ref.reshape(B, -1, ref.shape[1], ref.shape[2])
+    if ref.shape[1] == 1:
+        ref = np.repeat(ref, Hq, axis=1)
+    assert np.array_equal(vis.cpu().numpy(), ref)
+
+
+def test_varlen_full_lengths_equal_padded():
+    """Lengths equal to the padded sizes give bit-identical results to no lengths at all."""
+    B, Hq, Hkv, Sq, Sk, d = 2, 2, 2, 200, 450, 64
+    q, k, v = inp.qkv(B, Hq, Hkv, Sk, d, inp.F16, 11)
+    q = q[:, :, :Sq].contiguous().cuda()
+    k, v = k.cuda(), v.cuda()
+    outs = []
+    for lens in (None, (torch.full((B,), Sq, dtype=torch.int32, device="cuda"),
+                        torch.full((B,), Sk, dtype=torch.int32, device="cuda"))):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device="cuda")
+        af.attn_fwd_ex(q, k, v, o, lse, causal=True, seqlens_q=None if lens is None else lens[0],
+                       seqlens_k=None if lens is None else lens[1])
+        af.attn_check()
+        outs.append((o.cpu(), lse.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
