@@ -50,7 +50,7 @@ constexpr int QT = 2;          // Q tiles per work unit
 constexpr int UNIT_ROWS = BM * QT;
 constexpr int BN = 128;        // keys per K/V tile
 constexpr int NTHREADS = 384;  // 12 warps
-constexpr int REGS_LAUNCH = 168, REGS_LOADMMA = 80, REGS_SOFTMAX = 208;
+constexpr int REGS_LAUNCH = 168, REGS_LOADMMA = 88, REGS_SOFTMAX = 208;
 static_assert(128 * REGS_LOADMMA + 256 * REGS_SOFTMAX <= NTHREADS * REGS_LAUNCH, "register split");
 constexpr int NINFO = 4;       // depth of the tile-descriptor ring
 constexpr int TMEM_COLS = 512;
@@ -73,6 +73,11 @@ struct Layout {
   // d = 64 (short sequences, many units per CTA) double-buffers the Q tiles so the next
   // unit's Q load overlaps the current unit; d = 128 spends that room on K/V slots.
   static constexpr int QBUF = (D == 64) ? 2 : 1;
+  // With two Q buffers a unit's buffer is not refilled before the unit after next, so its
+  // epilogue can stage O there and write it out coalesced (8 softmax warps x 32 rows x d
+  // fp16/bf16 = exactly one buffer); the buffer is released when those warps are done.
+  static constexpr bool STAGE_O = (QBUF == 2);
+  static constexpr int QEMPTY_COUNT = 1 + (STAGE_O ? QT * 4 : 0);  // MMA commit + softmax warps
   // Separate K and V rings: K(j) is read by the two QK^T of tile j, V(j) by the two P.V
   // one tile later, so each ring is released right after its own last reader.
   static constexpr int KSLOT = (D == 128) ? (MODE == MASK_CUSTOM ? 2 : 3) : 4;
@@ -125,7 +130,7 @@ struct Params {
   int causal;      // the band only bounds keys on the right: longest units first
   int inject;
   float scale_log2;
-  unsigned long long timeout_ns;
+  uint32_t timeout_us;  // longest barrier wait (microseconds; 32 bits keep it in one register)
 };
 
 }  // namespace attn
@@ -137,14 +142,14 @@ namespace attn {
 
 // Slow path of a bounded barrier wait (inlined: a shared non-inlined callee cannot serve
 // warps running under different setmaxnreg budgets).  Gives up when another thread has aborted, when
-// the wait has lasted timeout_ns, or after an iteration cap, and then aborts the CTA.
+// the wait has lasted timeout_us, or after an iteration cap, and then aborts the CTA.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       unsigned long long timeout_ns) {
+                                       uint32_t timeout_us) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((it & 15u) == 15u && globaltimer_ns() - t0 > timeout_ns) break;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > 1000ull * timeout_us) break;
   }
   *abort_flag = 1;
   atomicOr(&g_attn_status, 1u);
@@ -152,15 +157,15 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatil
 }
 
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      unsigned long long timeout_ns) {
+                                      uint32_t timeout_us) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, timeout_ns);
+  return wait_slow(bar, parity, abort_flag, timeout_us);
 }
 
 // Warp-uniform variant: every lane waits, and the warp only proceeds if all lanes did.
 __device__ __forceinline__ bool bwait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           unsigned long long timeout_ns) {
-  bool ok = bwait(bar, parity, abort_flag, timeout_ns);
+                                           uint32_t timeout_us) {
+  bool ok = bwait(bar, parity, abort_flag, timeout_us);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -236,7 +241,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
                                           volatile int* abort_flag, int lane) {
   using L = Layout<D, MODE>;
   const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
-  const unsigned long long to = p.timeout_ns;
+  const uint32_t to = p.timeout_us;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
 
@@ -421,7 +426,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
                                          volatile int* abort_flag, uint32_t tmem, int lane) {
   using L = Layout<D, MODE>;
   const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
-  const unsigned long long to = p.timeout_ns;
+  const uint32_t to = p.timeout_us;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
   constexpr uint32_t ID_QK = idesc_f16acc32(BF16, false, false, BM, BN);
@@ -479,6 +484,9 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
                          (started || kk > 0) ? 1u : 0u);
           started = true;
         }
+        // end of unit: O_t is complete once its last P.V is -- signal it now, so softmax t
+        // starts its epilogue without waiting for the other Q tile's P.V
+        if (end && (t ? pv1 : pv0)) tc_commit_elect(bars + 8u * (L::B_ODONE + t));
         if (t == QT - 1 && have_prev) tc_commit_elect(bars + 8u * (L::B_VEMPTY + prev_vslot));
         if (!end && ((flags >> t) & 1)) {
           if (!k_ready) {
@@ -511,8 +519,6 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
       prev_vslot = cur_vslot;
       prev_vpar = cur_vpar;
     }
-    if (pv0) tc_commit_elect(bars + 8u * (L::B_ODONE + 0));
-    if (pv1) tc_commit_elect(bars + 8u * (L::B_ODONE + 1));
     tc_commit_elect(bars + 8u * (L::B_QEMPTY + qbuf));
   }
   return;
@@ -539,7 +545,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
   using L = Layout<D, MODE>;
   using OutT = uint16_t;
   const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
-  const unsigned long long to = p.timeout_ns;
+  const uint32_t to = p.timeout_us;
   const uint32_t bars = base + L::OFF_BAR;
   const uint32_t* words = reinterpret_cast<const uint32_t*>(gbase + L::OFF_WORDS);
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -641,17 +647,17 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       if (nact > 0 && __any_sync(0xffffffffu, grow)) {
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t ob[32];
-          tmem_ld32x32b_x32_wait(o_addr + ch * 32, ob);
+        for (int ch = 0; ch < D / 16; ++ch) {
+          uint32_t ob[16];
+          tmem_ld32x32b_x16_wait(o_addr + ch * 16, ob);
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
+          for (int x = 0; x < 8; ++x) {
             float lo, hi;
             f2_unpack(fmul2(f2_pack(__uint_as_float(ob[2 * x]), __uint_as_float(ob[2 * x + 1])), a2), lo, hi);
             ob[2 * x] = __float_as_uint(lo);
             ob[2 * x + 1] = __float_as_uint(hi);
           }
-          tmem_st32x32b_x32(o_addr + ch * 32, ob);
+          tmem_st32x32b_x16(o_addr + ch * 16, ob);
         }
       }
 
@@ -659,14 +665,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       const uint64_t c2 = f2_pack(c, c);
       const uint64_t nm2 = f2_pack(-m_use, -m_use);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-      // P_t goes over the first 64 columns of S_t, in two stores so the first overlaps
-      // the exponentials of the second half.
+      // P_t goes over the first 64 columns of S_t, in four stores so each overlaps the
+      // exponentials of the next quarter (and few packed words are live at a time).
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
+      for (int hh = 0; hh < 4; ++hh) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
-          const int e = hh * 32 + cc;
+        for (int cc = 0; cc < 16; ++cc) {
+          const int e = hh * 16 + cc;
           float e0, e1;
           f2_unpack(ffma2(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), c2, nm2), e0, e1);
           const float p0 = ex2_approx(e0);
@@ -674,7 +680,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
           acc[cc & 3] = fadd2(acc[cc & 3], f2_pack(p0, p1));
           pk[cc] = pack2<BF16>(p0, p1);
         }
-        tmem_st32x32b_x32(s_addr + hh * 32, pk);
+        tmem_st32x32b_x16(s_addr + hh * 16, pk);
       }
       tmem_wait_st();
       float s0, s1, s2, s3, s4, s5, s6, s7;
@@ -698,25 +704,67 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     }
     const bool row_ok = i < sq;
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (L::STAGE_O && nact > 0) {
+      // This warp's 32 rows x d go through its slice of the unit's Q buffer (the unit's
+      // last Q.K^T of tile t finished before O_t was signalled; a tile that computed
+      // nothing never waited for its Q load, so it writes its zeros directly instead):
+      // row r's 16-byte chunk c is stored at
+      // chunk c ^ (r & 7) of the slice's row r, so both the row-per-lane writes and the
+      // chunk-per-lane reads below touch every bank group once per 8 lanes.  The reads
+      // give each store instruction 512 contiguous bytes of O (4 whole rows).
+      constexpr int ROW_BYTES = D * 2, CHUNKS = ROW_BYTES / 16;
+      static_assert(QT * 4 * 32 * ROW_BYTES == L::Q_BUF_BYTES, "staging slices fill one Q buffer");
+      uint8_t* stage = gbase + L::OFF_Q + (k % L::QBUF) * L::Q_BUF_BYTES + (t * 4 + quarter) * (32 * ROW_BYTES);
+#pragma unroll
+      for (int ch = 0; ch < D / 16; ++ch) {
+        uint32_t ob[16];
+        tmem_ld32x32b_x16_wait(o_addr + ch * 16, ob);
+        uint32_t pk[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          pk[x] = pack2<BF16>(__uint_as_float(ob[2 * x]) * inv, __uint_as_float(ob[2 * x + 1]) * inv);
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          const int c = 2 * ch + hc;
+          *reinterpret_cast<uint4*>(stage + lane * ROW_BYTES + ((c ^ (lane & 7)) * 16)) =
+              make_uint4(pk[4 * hc], pk[4 * hc + 1], pk[4 * hc + 2], pk[4 * hc + 3]);
+        }
+      }
+      __syncwarp();
+      const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;  // this warp's first row
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + row0w) * ROW_BYTES;
+      constexpr int ROWS_PER_STORE = 32 / CHUNKS;
+#pragma unroll
+      for (int kk = 0; kk < 32 / ROWS_PER_STORE; ++kk) {
+        const int rr = kk * ROWS_PER_STORE + lane / CHUNKS, c = lane % CHUNKS;
+        const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * ROW_BYTES + ((c ^ (rr & 7)) * 16));
+        if (row0w + rr < sq) *reinterpret_cast<uint4*>(obase + rr * ROW_BYTES + c * 16) = val;
+      }
+      fence_proxy_async_smem();  // the next TMA load into this buffer comes after these accesses
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * (L::B_QEMPTY + (k % L::QBUF)));  // slice read back
+    } else {
     OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + (row_ok ? i : 0)) * D;
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t ob[32];
+    for (int ch = 0; ch < D / 16; ++ch) {
+      uint32_t ob[16];
       if (nact > 0) {
-        tmem_ld32x32b_x32_wait(o_addr + ch * 32, ob);
+        tmem_ld32x32b_x16_wait(o_addr + ch * 16, ob);
       } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) ob[x] = 0u;
+        for (int x = 0; x < 16; ++x) ob[x] = 0u;
       }
-      uint32_t pk[16];
+      uint32_t pk[8];
 #pragma unroll
-      for (int x = 0; x < 16; ++x)
+      for (int x = 0; x < 8; ++x)
         pk[x] = pack2<BF16>(__uint_as_float(ob[2 * x]) * inv, __uint_as_float(ob[2 * x + 1]) * inv);
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 16);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
+    }
+    if (L::STAGE_O && lane == 0) mbar_arrive(bars + 8u * (L::B_QEMPTY + (k % L::QBUF)));
     }
     if (row_ok && p.lse)
       p.lse[(size_t)(b * p.Hq + hq) * p.Sq + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
@@ -739,7 +787,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int qb2 = 0; qb2 < L::QBUF; ++qb2) {
       mbar_init(bars + 8u * (L::B_QFULL + qb2), 1);
-      mbar_init(bars + 8u * (L::B_QEMPTY + qb2), 1);
+      mbar_init(bars + 8u * (L::B_QEMPTY + qb2), L::QEMPTY_COUNT);
     }
     for (int s = 0; s < L::KSLOT; ++s) {
       mbar_init(bars + 8u * (L::B_KFULL + s), 1);
@@ -777,7 +825,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
 
   // Register rebalancing: the load / MMA warpgroup (warps 0-3) needs few registers, the
-  // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 80 + 256 x 208 + 1024.
+  // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 88 + 256 x 208 exactly.
   // Each setmaxnreg sits in the same branch as the code it budgets for.
   if (warp < 4) {
     setmaxnreg_dec<REGS_LOADMMA>();
@@ -1063,7 +1111,10 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   p.lens_k = a.seqlens_k;
   p.causal = (p.er >= 0 && p.wl < 0) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.timeout_ns = g_timeout_ns.load();
+  {
+    const unsigned long long us = (g_timeout_ns.load() + 999ull) / 1000ull;
+    p.timeout_us = us > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)us;
+  }
   p.inject = g_inject.exchange(0);
   const int grid = p.num_units < sms ? p.num_units : sms;
   const int mode = a.mask_bits                        ? MASK_CUSTOM
