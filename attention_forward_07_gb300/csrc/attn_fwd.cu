@@ -78,15 +78,21 @@ struct Layout {
   // fp16/bf16 = exactly one buffer); the buffer is released when those warps are done.
   static constexpr bool STAGE_O = (QBUF == 2);
   static constexpr int QEMPTY_COUNT = 1 + (STAGE_O ? QT * 4 : 0);  // MMA commit + softmax warps
+  // With one Q buffer (d = 128) the epilogue stages O through a 32 KiB area of its own,
+  // 4 KiB per softmax warp, one 64-column half at a time (custom masks need that room for
+  // their mask words and write O directly).
+  static constexpr bool STAGE_SEP = (D == 128 && MODE != MASK_CUSTOM);
+  static constexpr int STAGE_BYTES = STAGE_SEP ? QT * 4 * 32 * 128 : 0;
   // Separate K and V rings: K(j) is read by the two QK^T of tile j, V(j) by the two P.V
   // one tile later, so each ring is released right after its own last reader.
-  static constexpr int KSLOT = (D == 128) ? (MODE == MASK_CUSTOM ? 2 : 3) : 4;
+  static constexpr int KSLOT = (D == 128) ? 2 : 4;
   static constexpr int VSLOT = (D == 128) ? 2 : 4;
   static constexpr int OFF_Q = 0;
   static constexpr int Q_BUF_BYTES = QT * Q_TILE_BYTES;
   static constexpr int OFF_K = OFF_Q + QBUF * Q_BUF_BYTES;
   static constexpr int OFF_V = OFF_K + KSLOT * KV_TILE_BYTES;
-  static constexpr int OFF_WORDS = OFF_V + VSLOT * KV_TILE_BYTES;
+  static constexpr int OFF_STAGE = OFF_V + VSLOT * KV_TILE_BYTES;
+  static constexpr int OFF_WORDS = OFF_STAGE + STAGE_BYTES;
   static constexpr int WORDS_PER_ENTRY = UNIT_ROWS * (BN / 32);
   static constexpr int OFF_HDR = OFF_WORDS + (MODE == MASK_CUSTOM ? NINFO * WORDS_PER_ENTRY * 4 : 0);
   static constexpr int OFF_BAR = OFF_HDR + NINFO * 16;
@@ -459,6 +465,9 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
         if (++kslot == L::KSLOT) { kslot = 0; kpar ^= 1u; }
         if (++vslot == L::VSLOT) { vslot = 0; vpar ^= 1u; }
       }
+      // End of unit: every Q_t K^T of the unit is in the pipe, so the Q buffer is released
+      // (to the next unit's load) before the last P.V, which does not read it.
+      if (end) tc_commit_elect(bars + 8u * (L::B_QEMPTY + qbuf));
       if (have_prev) {
         if (!bwait_warp(bars + 8u * (L::B_VFULL + prev_vslot), prev_vpar, abort_flag, to)) goto drain;
         tc_fence_after();
@@ -519,7 +528,6 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
       prev_vslot = cur_vslot;
       prev_vpar = cur_vpar;
     }
-    tc_commit_elect(bars + 8u * (L::B_QEMPTY + qbuf));
   }
   return;
 
@@ -743,6 +751,43 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       fence_proxy_async_smem();  // the next TMA load into this buffer comes after these accesses
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8u * (L::B_QEMPTY + (k % L::QBUF)));  // slice read back
+    } else if (L::STAGE_SEP) {
+      // Same scheme through the warp's own 4 KiB slice, one 64-column half of d per pass:
+      // each store instruction then writes four whole 128-byte segments of O.
+      uint8_t* stage = gbase + L::OFF_STAGE + (t * 4 + quarter) * (32 * 128);
+      const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + row0w) * (D * 2);
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t ob[16];
+          if (nact > 0) {
+            tmem_ld32x32b_x16_wait(o_addr + h * 64 + ch * 16, ob);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) ob[x] = 0u;
+          }
+          uint32_t pk[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            pk[x] = pack2<BF16>(__uint_as_float(ob[2 * x]) * inv, __uint_as_float(ob[2 * x + 1]) * inv);
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {
+            const int c = 2 * ch + hc;
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * hc], pk[4 * hc + 1], pk[4 * hc + 2], pk[4 * hc + 3]);
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int rr = kk * 4 + lane / 8, c = lane % 8;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) * 16));
+          if (row0w + rr < sq) *reinterpret_cast<uint4*>(obase + rr * (D * 2) + h * 128 + c * 16) = val;
+        }
+        __syncwarp();  // the slice is rewritten by the next half
+      }
     } else {
     OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + (row_ok ? i : 0)) * D;
 #pragma unroll
