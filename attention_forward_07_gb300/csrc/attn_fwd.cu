@@ -868,6 +868,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Custom masks: the set-up above overlapped the mask pre-pass (dependent launch); its
+  // words and block flags are read only after this point.
+  if constexpr (MODE == MASK_CUSTOM) grid_dependency_wait();
 
   // Register rebalancing: the load / MMA warpgroup (warps 0-3) needs few registers, the
   // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 88 + 256 x 208 exactly.
@@ -909,42 +912,46 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 // per row, and a 1 into flags[(mb*nqt + qt)*nkt + kt] iff any of them is set.  The attention
 // kernel then reads only these: whole word tiles by TMA, and the emptiness flags for its
 // tile skipping.
-__global__ void __launch_bounds__(256) mask_prepass_kernel(const uint32_t* __restrict__ mask,
-                                                           uint32_t* __restrict__ words4,
-                                                           uint8_t* __restrict__ flags, Params p,
-                                                           int nmb) {
-  const long long gw_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (gw_id >= (long long)nmb * p.nqt * p.nkt) return;  // warp-uniform
-  const int kt = (int)(gw_id % p.nkt);
-  const long long rest = gw_id / p.nkt;
+__global__ void __launch_bounds__(BM) mask_prepass_kernel(const uint32_t* __restrict__ mask,
+                                                          uint32_t* __restrict__ words4,
+                                                          uint8_t* __restrict__ flags, Params p,
+                                                          int nmb) {
+  // One CTA per (mask row block, Q tile, key tile) block, one thread per query row: every
+  // thread's four words are loaded together, and the block's emptiness flag is a CTA-wide OR.
+  grid_launch_dependents();  // the attention grid may start its set-up; it waits for our output
+  const long long blk = blockIdx.x;  // grid = nmb * nqt * nkt exactly
+  const int kt = (int)(blk % p.nkt);
+  const long long rest = blk / p.nkt;
   const int qt = (int)(rest % p.nqt);
   const long long mbk = rest / p.nqt;
   const int W4 = 4 * p.nkt;
   int sq, sk;
   unit_lengths(p, (int)(mbk / p.mask_heads), sq, sk);
   const int off = sk - sq;
+  const int i = qt * BM + (int)threadIdx.x;
   uint32_t any = 0;
-#pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    const int i = qt * BM + rr * 32 + lane;
-    if (i >= p.Sq) continue;
+  if (i < p.Sq) {
     const uint32_t* src = mask + ((size_t)mbk * p.Sq + i) * p.W;
     uint32_t* dst = words4 + ((size_t)mbk * p.Sq + i) * W4;
     // rows past the entry's length keep nothing; keys past it do not exist
     const int klo = key_lo(p, i, off);
     const int khi = i < sq ? key_hi(p, i, off, sk) : 0;  // <= sk
+    uint32_t x[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const int gw = kt * 4 + w;
-      uint32_t x = 0;
-      if (gw < p.W) x = src[gw] & bit_range(klo - gw * 32, khi - gw * 32);
-      dst[gw] = x;
-      any |= x;
+      x[w] = gw < p.W ? __ldg(src + gw) : 0u;
     }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int gw = kt * 4 + w;
+      x[w] &= bit_range(klo - gw * 32, khi - gw * 32);
+      any |= x[w];
+    }
+    *reinterpret_cast<uint4*>(dst + kt * 4) = make_uint4(x[0], x[1], x[2], x[3]);
   }
-  const bool hit = __any_sync(0xffffffffu, any != 0u);
-  if (lane == 0) flags[gw_id] = hit ? 1 : 0;
+  const int hit = __syncthreads_or(any != 0u);
+  if (threadIdx.x == 0) flags[blk] = hit ? 1 : 0;
 }
 
 }  // namespace attn
@@ -1048,10 +1055,9 @@ int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream
   const MaskScratch ms(nmb, p.Sq, p.Sk);
   uint32_t* words4 = reinterpret_cast<uint32_t*>(scratch);
   uint8_t* flags = reinterpret_cast<uint8_t*>(scratch) + MaskScratch::round256(ms.words_bytes);
-  const long long warps = (long long)nmb * p.nqt * p.nkt;
-  const long long blocks = (warps * 32 + 255) / 256;
+  const long long blocks = (long long)nmb * p.nqt * p.nkt;
   if (blocks > INT_MAX) return ATTN_ERR_INVALID;
-  mask_prepass_kernel<<<(unsigned)blocks, 256, 0, st>>>(mask_bits, words4, flags, p, nmb);
+  mask_prepass_kernel<<<(unsigned)blocks, BM, 0, st>>>(mask_bits, words4, flags, p, nmb);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   p.tflags = flags;
   return make_mask_map(&p.tm_m, words4, 4 * p.nkt, p.Sq, nmb);
@@ -1068,6 +1074,20 @@ int launch(const Params& p, int grid, cudaStream_t st, int dev) {
         cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_set.fetch_or(bit);
+  }
+  if constexpr (MODE == MASK_CUSTOM) {
+    // Launched as a programmatic dependent of the mask pre-pass just enqueued on `st`.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = L::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
   kern<<<grid, NTHREADS, L::SMEM_ALLOC, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
