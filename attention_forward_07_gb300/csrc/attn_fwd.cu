@@ -7,11 +7,11 @@
 // One persistent CTA per SM, 384 threads, warp-specialised:
 //   warp 0       load warp: TMA loads of the two 128-row Q tiles of a work unit and of
 //                the K / V tiles into a ring of 128-byte-swizzled shared-memory slots;
-//                for custom masks it also stages the tile's mask words in shared memory
-//                and decides, with a warp ballot, which (Q tile, K tile) blocks hold a
-//                kept entry (the tile-skip ballot of the page "Opus 4.6 +
-//                AutoResearch驱动25轮迭代...", first excerpt).  Empty blocks are never
-//                loaded or computed.
+//                for custom masks it also stages the tile's kept-bit words in shared
+//                memory and decides, with a warp ballot over the block flags, which
+//                (Q tile, K tile) blocks hold a kept entry (the tile-skip ballot of the
+//                page "Opus 4.6 + AutoResearch驱动25轮迭代...", first excerpt).  Empty
+//                blocks are never loaded or computed.
 //   warp 1       MMA warp: one thread issues tcgen05.mma.  S_t = Q_t K^T (both operands in
 //                shared memory, fp32 accumulator in TMEM) and O_t += P_t V (P_t read from
 //                TMEM, V from shared memory), interleaved so the QK^T of the next key tile
@@ -24,6 +24,14 @@
 //                unit normalise O, store it and the LSE.
 // Work unit = (batch, query head, 256-row block); units are dealt to CTAs in a fixed
 // snake order; for causal masks the heaviest blocks (most key tiles) come first.
+// Custom masks go through two small kernels first: the pre-pass ANDs the caller's words
+// with the causal / window / length bounds into whole-tile words and flags each (16-row
+// block, key tile) pair that keeps anything; the compaction lists the 16-row blocks that
+// keep anything.  A unit then computes the next sixteen listed blocks as its two Q tiles
+// (gathered block by block, or loaded whole when they are its own rows) and writes O = 0,
+// LSE = -inf for the rows of its own blocks that keep nothing.  Both kernels let the next
+// grid start early (programmatic dependent launch) and the attention kernel waits for
+// their output with griddepcontrol.wait.
 // Every barrier wait is bounded: a wait that runs out sets a shared abort flag and the
 // device status word, every role drains what it has in flight and the CTA returns.
 
@@ -120,10 +128,19 @@ struct InfoHdr {
 
 struct Params {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps {d, S, B*H}, box {64, 128, 1}, 128B swizzle
-  CUtensorMap tm_m;              // kept-bit words {W4, S, B}, box {4, 256, 1} (custom masks)
+  CUtensorMap tm_m;              // kept-bit words {W4, S, nmb}, box {4, 16, 1} (custom masks)
+  CUtensorMap tm_q16;            // Q with 16-row boxes: gathers of compacted row blocks
+  CUtensorMap tm_m256;           // kept-bit words, box {4, 256, 1}: a unit whose slots are in place
   void* o;
   float* lse;
-  const uint8_t* tflags;  // [B][nqt][nkt] 1 = block holds a kept entry (custom masks)
+  // Custom masks (written by the mask kernels): the query rows of a mask row block mb with
+  // any kept entry, in 16-row blocks listed in ascending order and packed into 128-row
+  // compacted tiles; a work unit (b, hq, qb) computes compacted tiles 2 qb and 2 qb + 1 and
+  // owns the 16-row blocks of original rows [256 qb, 256 qb + 256) with nothing kept.
+  const uint8_t* tflags;  // [nmb][nqt][nkt] 1 = compacted tile holds a kept entry in key tile
+  const int* rowmap;      // [nmb][nqb * 16] original 16-row block of each compacted slot, -1 past the list
+  const uint8_t* live;    // [nmb][nr16] 1 = the 16-row block holds a kept entry
+  int nr16;               // ceil(Sq / 16)
   uint8_t* visited;
   int B, Hq, Hkv, Sq, Sk, g, nqb, nkt, nqt, W, num_units;
   // Query row i of a batch entry with sq queries and sk keys sits at key position
@@ -270,15 +287,39 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     decode_unit(u, p, causal, b, hq, qb);
     const int hkv = hq / p.g;
     const int row0 = qb * UNIT_ROWS;
+    const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
+    // Custom masks: lane s < 16 holds the original 16-row block of compacted slot s of the
+    // unit (-1: none), and the unit has nothing to compute when its first slot is empty.
+    int slot_blk = -1;
+    bool unit_empty = false, in_place = true;
+    if constexpr (MODE == MASK_CUSTOM) {
+      if (lane < 2 * QT * 4) slot_blk = __ldg(p.rowmap + ((size_t)mb * p.nqb + qb) * 16 + lane);
+      unit_empty = __shfl_sync(0xffffffffu, slot_blk, 0) < 0;
+      // slots that are the unit's own rows (no empty block among them): plain tile loads
+      const int own = qb * 16 + lane;
+      in_place = __all_sync(0xffffffffu, lane >= 2 * QT * 4 || slot_blk == (own < p.nr16 ? own : -1));
+    }
 
-    // Both Q tiles of the unit (rows past S are zero-filled by the TMA unit).
+    // Both Q tiles of the unit (rows past S are zero-filled by the TMA unit).  Custom masks
+    // gather them block by block from the compacted list (a missing block reads as zeros).
     const int qbuf = k % L::QBUF;
     if (!bwait_warp(bars + 8u * (L::B_QEMPTY + qbuf), (q_empty_par >> qbuf) & 1u, abort_flag, to))
       goto drain;
     q_empty_par ^= 1u << qbuf;
     if (!inject) {
-      if (lane == 0) {
-        const uint32_t fb = bars + 8u * (L::B_QFULL + qbuf);
+      const uint32_t fb = bars + 8u * (L::B_QFULL + qbuf);
+      if (MODE == MASK_CUSTOM && !in_place) {
+        if (lane == 0) mbar_expect_tx(fb, unit_empty ? 0u : (uint32_t)L::Q_BUF_BYTES);
+        __syncwarp();
+        if (!unit_empty && lane < 2 * QT * 4) {
+          const int t = lane >> 3, blk = lane & 7;
+          const int y = slot_blk >= 0 ? slot_blk * 16 : p.Sq;  // past Sq: zero fill
+#pragma unroll
+          for (int h = 0; h < L::HALVES; ++h)
+            tma_load_3d(base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES + h * BM * 128 + blk * 16 * 128,
+                        &p.tm_q16, fb, h * 64, y, b * p.Hq + hq);
+        }
+      } else if (lane == 0) {
         mbar_expect_tx(fb, L::Q_BUF_BYTES);
 #pragma unroll
         for (int t = 0; t < QT; ++t)
@@ -309,10 +350,15 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       const bool any = r0 < sq && rf <= r1 && khi > klo;
       jlo[t] = any ? klo / BN : 0;
       jhi[t] = any ? (khi - 1) / BN : -1;  // -1: nothing to compute for this Q tile
+      if constexpr (MODE == MASK_CUSTOM) {
+        // compacted tiles: every key tile, the flags decide (band and lengths are in them)
+        const bool valid = __shfl_sync(0xffffffffu, slot_blk, t * 8) >= 0;
+        jlo[t] = 0;
+        jhi[t] = valid ? p.nkt - 1 : -1;
+      }
     }
     const int jbeg = jhi[0] < 0 ? jlo[1] : (jhi[1] < 0 ? jlo[0] : min(jlo[0], jlo[1]));
     const int jend = max(jhi[0], jhi[1]) + 1;
-    const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
     uint32_t f0 = 0, f1 = 0;  // bit (j % 32): Q tile 0 / 1 has a kept entry in key tile j
     for (int j = jbeg; j < jend; ++j) {
       bool a0 = j >= jlo[0] && j <= jhi[0];
@@ -344,12 +390,21 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
         hdr[ie].sk = sk;
         const uint32_t fb = bars + 8u * (L::B_IFULL + ie);
         if constexpr (MODE == MASK_CUSTOM) {
-          // the block's kept-bit words (256 rows x 4 words) land in the descriptor slot
           mbar_expect_tx(fb, L::WORDS_PER_ENTRY * 4);
-          tma_load_3d(base + L::OFF_WORDS + ie * L::WORDS_PER_ENTRY * 4, &p.tm_m, fb,
-                      j * (BN / 32), row0, mb);
         } else {
           mbar_arrive(fb);
+        }
+      }
+      if constexpr (MODE == MASK_CUSTOM) {
+        // the kept-bit words of the unit's 16 compacted slots (16 rows x 4 words each) land
+        // in the descriptor slot in compacted row order; a missing block reads as zeros
+        __syncwarp();
+        const uint32_t wdst = base + L::OFF_WORDS + ie * L::WORDS_PER_ENTRY * 4;
+        if (in_place) {
+          if (lane == 0) tma_load_3d(wdst, &p.tm_m256, bars + 8u * (L::B_IFULL + ie), j * (BN / 32), row0, mb);
+        } else if (lane < 2 * QT * 4) {
+          tma_load_3d(wdst + lane * 16 * (BN / 32) * 4, &p.tm_m, bars + 8u * (L::B_IFULL + ie), j * (BN / 32),
+                      slot_blk >= 0 ? slot_blk * 16 : p.Sq, mb);
         }
       }
       if constexpr (MODE == MASK_CUSTOM) {
@@ -571,7 +626,18 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     if (u < 0) break;
     int b, hq, qb;
     decode_unit(u, p, causal, b, hq, qb);
-    const int i = qb * UNIT_ROWS + t * BM + r;
+    const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
+    // This thread's query row.  Custom masks: the tile holds compacted slots, 16 rows each;
+    // blk_a / blk_b are the original blocks of this warp's two slots (-1: no such slot).
+    int i = qb * UNIT_ROWS + t * BM + r;
+    int blk_a = 0, blk_b = 0;
+    if constexpr (MODE == MASK_CUSTOM) {
+      const int* rm = p.rowmap + ((size_t)mb * p.nqb + qb) * 16 + t * 8 + quarter * 2;
+      blk_a = __ldg(rm);
+      blk_b = __ldg(rm + 1);
+      const int blk = lane < 16 ? blk_a : blk_b;
+      i = blk >= 0 ? blk * 16 + (lane & 15) : -1;
+    }
     float m = -INFINITY, l = 0.f;
     int nact = 0;
     int sq = p.Sq, sk = p.Sk;  // the unit's lengths, carried by every tile descriptor
@@ -710,7 +776,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       o_par ^= 1u;
       tc_fence_after();
     }
-    const bool row_ok = i < sq;
+    const bool row_ok = i >= 0 && i < sq;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     if (L::STAGE_O && nact > 0) {
       // This warp's 32 rows x d go through its slice of the unit's Q buffer (the unit's
@@ -740,13 +806,18 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       }
       __syncwarp();
       const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;  // this warp's first row
-      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + row0w) * ROW_BYTES;
+      uint8_t* obh = reinterpret_cast<uint8_t*>(p.o) + (size_t)(b * p.Hq + hq) * p.Sq * ROW_BYTES;
       constexpr int ROWS_PER_STORE = 32 / CHUNKS;
 #pragma unroll
       for (int kk = 0; kk < 32 / ROWS_PER_STORE; ++kk) {
         const int rr = kk * ROWS_PER_STORE + lane / CHUNKS, c = lane % CHUNKS;
         const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * ROW_BYTES + ((c ^ (rr & 7)) * 16));
-        if (row0w + rr < sq) *reinterpret_cast<uint4*>(obase + rr * ROW_BYTES + c * 16) = val;
+        int orow = row0w + rr;  // the slice row's place in O
+        if constexpr (MODE == MASK_CUSTOM) {
+          const int blk = rr < 16 ? blk_a : blk_b;
+          orow = blk >= 0 ? blk * 16 + (rr & 15) : -1;
+        }
+        if (orow >= 0 && orow < sq) *reinterpret_cast<uint4*>(obh + (size_t)orow * ROW_BYTES + c * 16) = val;
       }
       fence_proxy_async_smem();  // the next TMA load into this buffer comes after these accesses
       __syncwarp();
@@ -813,6 +884,25 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     }
     if (row_ok && p.lse)
       p.lse[(size_t)(b * p.Hq + hq) * p.Sq + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+    if constexpr (MODE == MASK_CUSTOM) {
+      // The unit also owns the 16-row blocks of its original rows; those with nothing kept
+      // were left out of the compacted list: O = 0 and LSE = -inf there, this warp's two
+      // blocks written in whole 16-byte chunks by consecutive lanes.
+      constexpr int ROW_BYTES = D * 2, CHUNKS = ROW_BYTES / 16;
+      const int hb0 = (qb * UNIT_ROWS + t * BM + quarter * 32) / 16;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int hb = hb0 + hh;
+        if (hb >= p.nr16 || __ldg(p.live + (size_t)mb * p.nr16 + hb)) continue;  // warp-uniform
+        uint8_t* ob = reinterpret_cast<uint8_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + hb * 16) * ROW_BYTES;
+#pragma unroll
+        for (int q = lane; q < 16 * CHUNKS; q += 32) {
+          const int rr = q / CHUNKS, c = q % CHUNKS;
+          if (hb * 16 + rr < sq) *reinterpret_cast<uint4*>(ob + rr * ROW_BYTES + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (lane < 16 && hb * 16 + lane < sq && p.lse) p.lse[(size_t)(b * p.Hq + hq) * p.Sq + hb * 16 + lane] = -INFINITY;
+      }
+    }
   }
 }
 
@@ -914,10 +1004,11 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 // tile skipping.
 __global__ void __launch_bounds__(BM) mask_prepass_kernel(const uint32_t* __restrict__ mask,
                                                           uint32_t* __restrict__ words4,
-                                                          uint8_t* __restrict__ flags, Params p,
+                                                          uint8_t* __restrict__ flags16, Params p,
                                                           int nmb) {
-  // One CTA per (mask row block, Q tile, key tile) block, one thread per query row: every
-  // thread's four words are loaded together, and the block's emptiness flag is a CTA-wide OR.
+  // One CTA per (mask row block, 128 query rows, key tile), one thread per query row: every
+  // thread's four words are loaded together; each half-warp's OR is the emptiness flag of
+  // one (16-row block, key tile) pair.
   grid_launch_dependents();  // the attention grid may start its set-up; it waits for our output
   const long long blk = blockIdx.x;  // grid = nmb * nqt * nkt exactly
   const int kt = (int)(blk % p.nkt);
@@ -950,8 +1041,71 @@ __global__ void __launch_bounds__(BM) mask_prepass_kernel(const uint32_t* __rest
     }
     *reinterpret_cast<uint4*>(dst + kt * 4) = make_uint4(x[0], x[1], x[2], x[3]);
   }
-  const int hit = __syncthreads_or(any != 0u);
-  if (threadIdx.x == 0) flags[blk] = hit ? 1 : 0;
+  const uint32_t bits = __ballot_sync(0xffffffffu, any != 0u);
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r16 = qt * (BM / 16) + (int)(threadIdx.x >> 5) * 2 + h;
+      if (r16 < p.nr16) flags16[((size_t)mbk * p.nr16 + r16) * p.nkt + kt] = ((bits >> (16 * h)) & 0xFFFFu) ? 1 : 0;
+    }
+  }
+}
+
+// Compaction of one mask row block (one CTA per block, 256 threads): which 16-row blocks
+// hold a kept entry, their ascending list (the compacted slots, -1 past its end), and the
+// (compacted tile, key tile) flags as the OR over the tile's eight slots.  Shared memory:
+// nslots (>= nqt * 8 >= nr16) slot entries and nr16 bytes of liveness.
+__global__ void __launch_bounds__(256) mask_compact_kernel(const uint8_t* __restrict__ flags16,
+                                                          uint8_t* __restrict__ live, int* __restrict__ rowmap,
+                                                          uint8_t* __restrict__ tflags, int nr16, int nkt,
+                                                          int nqt, int nslots) {
+  grid_launch_dependents();  // the attention grid may start its set-up; it waits for our output
+  grid_dependency_wait();    // launched as a dependent of the pre-pass: its flags are complete
+  extern __shared__ int cmp_smem[];
+  int* slot_s = cmp_smem;                                             // nslots
+  uint8_t* live_s = reinterpret_cast<uint8_t*>(cmp_smem + nslots);    // nr16
+  __shared__ int warp_tot[8];
+  __shared__ int carry_s;
+  const int mb = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint8_t* f = flags16 + (size_t)mb * nr16 * nkt;
+  for (int r = tid; r < nr16; r += 256) {
+    uint32_t any = 0;
+    for (int kt = 0; kt < nkt; ++kt) any |= f[(size_t)r * nkt + kt];
+    live_s[r] = any ? 1 : 0;
+    live[(size_t)mb * nr16 + r] = any ? 1 : 0;
+  }
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  // ascending list of the live blocks: a block-wide exclusive scan, 256 blocks per round
+  for (int base = 0; base < nr16; base += 256) {
+    const int r = base + tid;
+    const bool v = r < nr16 && live_s[r];
+    const uint32_t bal = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) warp_tot[warp] = __popc(bal);
+    __syncthreads();
+    int before = carry_s;
+    for (int w = 0; w < warp; ++w) before += warp_tot[w];
+    if (v) slot_s[before + __popc(bal & ((1u << lane) - 1u))] = r;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < 8; ++w) tot += warp_tot[w];
+      carry_s += tot;
+    }
+    __syncthreads();
+  }
+  const int c = carry_s;
+  for (int sl = tid; sl < nslots; sl += 256) {
+    if (sl >= c) slot_s[sl] = -1;
+    rowmap[(size_t)mb * nslots + sl] = sl < c ? slot_s[sl] : -1;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nqt * nkt; idx += 256) {
+    const int ct = idx / nkt, kt = idx % nkt;
+    uint32_t any = 0;
+    for (int sl = ct * 8; sl < ct * 8 + 8 && sl < c; ++sl) any |= f[(size_t)slot_s[sl] * nkt + kt];
+    tflags[(size_t)mb * nqt * nkt + idx] = any ? 1 : 0;
+  }
 }
 
 }  // namespace attn
@@ -1004,14 +1158,14 @@ int device_info(int& sms, int& dev) {
   return ATTN_OK;
 }
 
-// [rows = B*H][S][d] tensor as a 3-D map {d, S, B*H}; box {64, 128, 1}: one 128-byte
-// swizzle span of 128 rows.  Rows past S read as zeros.
-int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long BH) {
+// [rows = B*H][S][d] tensor as a 3-D map {d, S, B*H}; box {64, box_rows, 1}: one 128-byte
+// swizzle span of box_rows rows.  Rows past S read as zeros.
+int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long BH, int box_rows = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * (cuuint64_t)d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1020,14 +1174,15 @@ int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Kept-bit words of a custom mask after the pre-pass: 3-D map {W4, S, B} of uint32, box
-// {4 words, 256 rows, 1}: one key tile's words for the 256 rows of a work unit.
-int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nmb) {
+// Kept-bit words of a custom mask after the pre-pass: 3-D map {W4, S, nmb} of uint32, box
+// {4 words, box_rows, 1}: one key tile's words for one 16-row block (gathered per slot) or
+// for the 256 rows of a unit whose compacted slots are its own rows.
+int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nmb, int box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)W4, (cuuint64_t)Sq, (cuuint64_t)nmb};
   cuuint64_t strides[2] = {(cuuint64_t)W4 * 4, (cuuint64_t)Sq * (cuuint64_t)W4 * 4};
-  cuuint32_t box[3] = {BN / 32, UNIT_ROWS, 1};
+  cuuint32_t box[3] = {BN / 32, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(words4), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1039,28 +1194,71 @@ int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nm
 // masks): padded kept-bit words [nmb][Sq][W4] then the block emptiness flags
 // [nmb][nqt][nkt].
 struct MaskScratch {
-  size_t words_bytes, flags_bytes;
+  // kept-bit words [nmb][Sq][W4], flags per (16-row block, key tile) [nmb][nr16][nkt],
+  // live 16-row blocks [nmb][nr16], compacted slot -> block [nmb][nqb * 16] (int, 16 slots per
+  // 256-row work unit), compacted tile flags [nmb][nqt][nkt]; every part starts on a 256-byte
+  // boundary
+  size_t off_flags16, off_live, off_rowmap, off_tflags, bytes;
   static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
   MaskScratch(long long nmb, int Sq, int Sk) {
-    const long long nqt = (Sq + BM - 1) / BM, nkt = (Sk + BN - 1) / BN;
-    words_bytes = (size_t)nmb * Sq * (size_t)(4 * nkt) * 4;
-    flags_bytes = (size_t)(nmb * nqt * nkt);
+    const long long nqt = (Sq + BM - 1) / BM, nkt = (Sk + BN - 1) / BN, nr16 = (Sq + 15) / 16;
+    const long long nslots = (Sq + UNIT_ROWS - 1) / UNIT_ROWS * 16;
+    off_flags16 = round256((size_t)nmb * Sq * (size_t)(4 * nkt) * 4);
+    off_live = off_flags16 + round256((size_t)(nmb * nr16 * nkt));
+    off_rowmap = off_live + round256((size_t)(nmb * nr16));
+    off_tflags = off_rowmap + round256((size_t)(nmb * nslots) * 4);
+    bytes = off_tflags + round256((size_t)(nmb * nqt * nkt));
   }
-  size_t total() const { return round256(words_bytes) + flags_bytes; }
+  size_t total() const { return bytes; }
 };
 
 // Runs the mask pre-pass into `scratch` (MaskScratch layout) and points p at its output.
-int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream_t st) {
+int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream_t st, int dev) {
   const int nmb = p.B * p.mask_heads;
   const MaskScratch ms(nmb, p.Sq, p.Sk);
-  uint32_t* words4 = reinterpret_cast<uint32_t*>(scratch);
-  uint8_t* flags = reinterpret_cast<uint8_t*>(scratch) + MaskScratch::round256(ms.words_bytes);
+  uint8_t* base = reinterpret_cast<uint8_t*>(scratch);
+  uint32_t* words4 = reinterpret_cast<uint32_t*>(base);
+  uint8_t* flags16 = base + ms.off_flags16;
+  uint8_t* live = base + ms.off_live;
+  int* rowmap = reinterpret_cast<int*>(base + ms.off_rowmap);
+  uint8_t* tflags = base + ms.off_tflags;
   const long long blocks = (long long)nmb * p.nqt * p.nkt;
   if (blocks > INT_MAX) return ATTN_ERR_INVALID;
-  mask_prepass_kernel<<<(unsigned)blocks, BM, 0, st>>>(mask_bits, words4, flags, p, nmb);
+  const int nslots = p.nqb * 16;
+  const size_t cmp_smem = (size_t)nslots * 4 + (size_t)p.nr16;
+  if (cmp_smem > 227 * 1024) return ATTN_ERR_UNSUPPORTED;
+  if (cmp_smem > 48 * 1024) {
+    static std::atomic<unsigned long long> attr_set{0};  // bit per device
+    const unsigned long long bit = 1ull << dev;
+    if (!(attr_set.load() & bit)) {
+      if (cudaFuncSetAttribute(mask_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+          cudaSuccess)
+        return ATTN_ERR_CUDA;
+      attr_set.fetch_or(bit);
+    }
+  }
+  mask_prepass_kernel<<<(unsigned)blocks, BM, 0, st>>>(mask_bits, words4, flags16, p, nmb);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  p.tflags = flags;
-  return make_mask_map(&p.tm_m, words4, 4 * p.nkt, p.Sq, nmb);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nmb);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = cmp_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mask_compact_kernel, (const uint8_t*)flags16, live, rowmap, tflags, p.nr16, p.nkt,
+                           p.nqt, nslots) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  p.tflags = tflags;
+  p.rowmap = rowmap;
+  p.live = live;
+  int rc = make_mask_map(&p.tm_m, words4, 4 * p.nkt, p.Sq, nmb, 16);
+  return rc != ATTN_OK ? rc : make_mask_map(&p.tm_m256, words4, 4 * p.nkt, p.Sq, nmb, UNIT_ROWS);
 }
 
 template <int D, bool BF16, int MODE>
@@ -1155,6 +1353,8 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   if ((rc = make_map(&p.tm_q, a.q, bf16, a.d, a.Sq, (long long)a.B * a.Hq)) != ATTN_OK) return rc;
   if ((rc = make_map(&p.tm_k, a.k, bf16, a.d, a.Sk, (long long)a.B * a.Hkv)) != ATTN_OK) return rc;
   if ((rc = make_map(&p.tm_v, a.v, bf16, a.d, a.Sk, (long long)a.B * a.Hkv)) != ATTN_OK) return rc;
+  if (a.mask_bits && (rc = make_map(&p.tm_q16, a.q, bf16, a.d, a.Sq, (long long)a.B * a.Hq, 16)) != ATTN_OK)
+    return rc;
   p.o = a.o;
   p.lse = a.lse;
   p.visited = a.visited;
@@ -1167,6 +1367,7 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   p.nqb = (int)nqb;
   p.nkt = (a.Sk + BN - 1) / BN;
   p.nqt = (a.Sq + BM - 1) / BM;
+  p.nr16 = (a.Sq + 15) / 16;
   p.W = (a.Sk + 31) / 32;
   p.num_units = a.B * a.Hq * (int)nqb;
   p.wl = a.window_left;
@@ -1201,7 +1402,7 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
       if (cudaMallocAsync(&scratch, need, st) != cudaSuccess) return ATTN_ERR_CUDA;
       owned = true;
     }
-    rc = prepare_mask(p, a.mask_bits, scratch, st);
+    rc = prepare_mask(p, a.mask_bits, scratch, st, dev);
   }
   if (rc == ATTN_OK) {
     if (a.d == 64)

@@ -35,10 +35,17 @@
  *   - Ownership: the caller owns every buffer; the library keeps no pointer
  *     after the call returns.  Without a custom mask nothing is allocated.  With
  *     one, a pre-pass kernel writes the kept-bit words (mask AND causal AND the
- *     key bound, padded to whole 128-column tiles) and a per-block emptiness map
- *     into stream-ordered scratch -- cudaMallocAsync / cudaFreeAsync on `stream`,
- *     B*S*ceil(S/128)*16 + B*ceil(S/128)^2 bytes (plus alignment) -- that the
- *     attention kernel reads and that is released in stream order after it.
+ *     key bound, padded to whole 128-column tiles) and an emptiness map per
+ *     (16-row block, 128-column tile), and a compaction kernel lists, per mask row
+ *     block, the 16-row blocks that keep anything: the attention kernel computes
+ *     only those, packed eight to a 128-row tile, and writes O = 0, LSE = -inf for
+ *     the rows of the others without computing them.  All of it lives in
+ *     stream-ordered scratch -- cudaMallocAsync / cudaFreeAsync on `stream` -- of
+ *     the "custom-mask scratch size": with nm mask row blocks (B, or B*Hq for
+ *     per-head masks), R = ceil(Sq/16), T = ceil(Sq/128), U = ceil(Sq/256) and
+ *     N = ceil(Sk/128), the sum of nm*Sq*N*16, nm*R*N, nm*R, nm*U*64 and nm*T*N
+ *     bytes, each rounded up to a multiple of 256 (Sq = Sk = S for attn_fwd).
+ *     It is released in stream order after the attention kernel.
  *   - Errors: arguments are validated before any launch (ATTN_ERR_INVALID /
  *     ATTN_ERR_UNSUPPORTED, nothing launched); a failed launch returns
  *     ATTN_ERR_CUDA.  The work is asynchronous: a kernel that gives up on a
@@ -96,8 +103,8 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *     past sk_b get weight exactly 0, so v must hold finite values there (0 * inf is NaN);
  *     k there may hold anything.  The custom-mask layout keeps the padded shape.
  * With Sq = Sk = S, windows -1, mask_per_head = 0 and no lengths it is attn_fwd.  Custom masks take
- * stream-ordered scratch of nm*Sq*ceil(Sk/128)*16 + nm*ceil(Sq/128)*ceil(Sk/128) bytes,
- * nm = B (or B*Hq per head).  Errors as for attn_fwd; Sk < Sq is ATTN_ERR_INVALID.
+ * stream-ordered scratch of the custom-mask scratch size above.  Errors as for attn_fwd;
+ * Sk < Sq is ATTN_ERR_INVALID.
  */
 typedef struct {
     const void *q, *k, *v;
@@ -123,8 +130,11 @@ int attn_fwd_ex(const attn_fwd_params_t *params);
  * attn_tile_shape.  The caller zeroes `visited`.  Blocks that hold no kept
  * entry -- every mask word over the block is zero, or the block lies above the
  * causal diagonal -- are skipped, following the tile-skip ballot of the page
- * "Opus 4.6 + AutoResearch驱动25轮迭代..." (first code excerpt).  O and LSE are
- * identical to attn_fwd's.
+ * "Opus 4.6 + AutoResearch驱动25轮迭代..." (first code excerpt).  With a custom mask
+ * qt numbers the compacted query tiles instead: tile qt holds the 16-row blocks
+ * 8*qt .. 8*qt+7 of the ascending list of blocks that keep anything (of batch
+ * entry b, or of head (b, hq) for per-head masks).  O and LSE are identical to
+ * attn_fwd's.
  */
 int attn_fwd_visited(const void *q, const void *k, const void *v, void *o, float *lse,
                      const uint32_t *mask_bits, int B, int Hq, int Hkv, int S, int d,
@@ -140,8 +150,8 @@ int attn_fwd_visited(const void *q, const void *k, const void *v, void *o, float
  * mask the two are the same call.  With one, the mask pre-pass output goes into a
  * fixed device array of ATTN_NOALLOC_SCRATCH_BYTES that this library reserves on
  * every GPU that loads it, held until the process exits, instead of into
- * stream-ordered scratch; calls whose B*S*ceil(S/128)*16 + B*ceil(S/128)^2
- * bytes (plus alignment) exceed it return ATTN_ERR_INVALID before any launch.
+ * stream-ordered scratch; calls whose custom-mask scratch size (see the
+ * conventions above) exceeds it return ATTN_ERR_INVALID before any launch.
  * The first call on a device looks the array's device address up (once, with
  * that device current); make that first call before any stream capture.  Every
  * call shares the one array and it keeps the last call's contents (each call

@@ -56,3 +56,28 @@ def assert_close(o, lse, o_ref, lse_ref, what=""):
     if (~neg).any():
         err = np.abs(lse[~neg] - lse_ref[~neg]).max()
         assert err <= LSE_ATOL, f"{what}: LSE error {err}"
+
+
+def expected_visited(bits, per_head, B, Hq, Sq, Sk, causal, window_left=-1, window_right=-1, seqlens_q=None,
+                     seqlens_k=None):
+    """The visited map the kernel must produce, uint8 [B, Hq, ceil(Sq/128), ceil(Sk/128)].
+
+    Without a custom mask: the oracle's (128-row, 128-key) block map.  With one, the kernel
+    first compacts the query rows: the 16-row blocks that hold a kept entry, in ascending
+    order, eight to a 128-row tile; a (compacted tile, key tile) block is visited iff one of
+    its 16-row blocks holds a kept entry in that key tile -- built here from the oracle's
+    (16-row, 128-key) block map."""
+    nqt, nkt = -(-Sq // 128), -(-Sk // 128)
+    if bits is None:
+        ref = oracle.skip_map_ex(None, False, B, Hq, Sq, Sk, causal, window_left, window_right, 128, 128,
+                                 seqlens_q=seqlens_q, seqlens_k=seqlens_k)
+        return np.repeat(ref.reshape(B, 1, nqt, nkt), Hq, axis=1)
+    f16 = oracle.skip_map_ex(bits, per_head, B, Hq, Sq, Sk, causal, window_left, window_right, 16, 128,
+                             seqlens_q=seqlens_q, seqlens_k=seqlens_k)
+    out = np.zeros((f16.shape[0], nqt, nkt), np.uint8)
+    for mb in range(f16.shape[0]):
+        blocks = np.nonzero(f16[mb].any(axis=1))[0]
+        for ct in range(-(-len(blocks) // 8)):
+            out[mb, ct] = f16[mb, blocks[ct * 8:(ct + 1) * 8]].any(axis=0)
+    out = out.reshape(B, -1, nqt, nkt)
+    return out if out.shape[1] == Hq else np.repeat(out, Hq, axis=1)

@@ -8,7 +8,7 @@ import attention_forward_07_gb300 as af
 import oracle
 from attention_forward_07_gb300 import inputs as inp
 
-from gpu_util import assert_close
+from gpu_util import assert_close, expected_visited
 
 pytestmark = pytest.mark.gpu
 
@@ -38,6 +38,11 @@ CASES = [
     (2, 4, 2, 256, 384, 64, inp.F16, True, -1, -1, "shared"),      # custom mask, Sq < Sk
     (2, 4, 2, 300, 300, 128, inp.BF16, True, 120, -1, "head"),     # per-head mask + window
     (1, 4, 4, 129, 640, 64, inp.F16, False, -1, -1, "head"),       # per-head, ragged
+    # masks with whole empty 16-row blocks: the rows are compacted before the tiles are formed
+    (2, 4, 2, 512, 512, 64, inp.F16, False, -1, -1, "sparse"),
+    (2, 2, 2, 700, 900, 128, inp.BF16, True, -1, -1, "sparse"),
+    (1, 4, 4, 333, 333, 64, inp.F16, True, 90, -1, "sparse_head"),
+    (2, 2, 1, 1100, 1100, 128, inp.BF16, False, 200, 100, "sparse"),
 ]
 
 
@@ -54,16 +59,17 @@ def test_extended_parity_and_skip_map(case):
     elif mask == "head":
         keep = inp.bernoulli_mask(B * Hq, Sk, 4)[:, :Sq]
         bits = inp.pack_bits(keep).reshape(B, Hq, Sq, -1)
+    elif mask == "sparse":
+        bits = inp.pack_bits(inp.block_sparse_mask(B, Sk, 7)[:, :Sq])
+    elif mask == "sparse_head":
+        per_head = True
+        bits = inp.pack_bits(inp.block_sparse_mask(B * Hq, Sk, 8)[:, :Sq]).reshape(B, Hq, Sq, -1)
     scale = 1.0 / d ** 0.5
     o, lse, vis = _run(q, k, v, bits, per_head, causal, wl, wr, scale, visited=True)
     o_ref, lse_ref = oracle.attn_rows_ex(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), dtype, None, bits,
                                          per_head, causal, wl, wr, float(np.float32(scale)))
     assert_close(o, lse, o_ref, lse_ref, str(case))
-    ref = oracle.skip_map_ex(bits, per_head, B, Hq, Sq, Sk, causal, wl, wr, 128, 128)
-    ref = ref.reshape(B, -1, ref.shape[1], ref.shape[2])
-    if ref.shape[1] == 1:
-        ref = np.repeat(ref, Hq, axis=1)
-    assert np.array_equal(vis, ref)
+    assert np.array_equal(vis, expected_visited(bits, per_head, B, Hq, Sq, Sk, causal, wl, wr))
 
 
 def test_ex_defaults_are_attn_fwd():
@@ -89,6 +95,7 @@ VARLEN_CASES = [
     (3, 2, 2, 384, 700, 128, inp.F16, False, 90, 20, None),
     (4, 2, 1, 260, 400, 64, inp.BF16, True, -1, -1, "shared"),
     (3, 4, 4, 200, 333, 128, inp.BF16, True, 64, -1, "head"),
+    (4, 2, 2, 600, 600, 64, inp.F16, True, -1, -1, "sparse"),
 ]
 
 
@@ -122,6 +129,8 @@ def test_varlen_parity_and_skip_map(case):
         bits = inp.pack_bits(inp.bernoulli_mask(B, Sk, 5)[:, :Sq])
     elif mask == "head":
         bits = inp.pack_bits(inp.bernoulli_mask(B * Hq, Sk, 6)[:, :Sq]).reshape(B, Hq, Sq, -1)
+    elif mask == "sparse":
+        bits = inp.pack_bits(inp.block_sparse_mask(B, Sk, 9)[:, :Sq])
     k_nan = k.clone()
     for b in range(B):
         k_nan[b, :, int(lk[b]):] = float("nan")
@@ -144,11 +153,8 @@ def test_varlen_parity_and_skip_map(case):
         assert np.all(np.isnan(o[b, :, n:])) and np.all(np.isnan(lse[b, :, n:])), f"entry {b}: padded rows written"
         if n:
             assert_close(o[b, :, :n], lse[b, :, :n], o_ref[b, :, :n], lse_ref[b, :, :n], f"{case} entry {b}")
-    ref = oracle.skip_map_ex(bits, per_head, B, Hq, Sq, Sk, causal, wl, wr, 128, 128, seqlens_q=lq, seqlens_k=lk)
-    ref = ref.reshape(B, -1, ref.shape[1], ref.shape[2])
-    if ref.shape[1] == 1:
-        ref = np.repeat(ref, Hq, axis=1)
-    assert np.array_equal(vis.cpu().numpy(), ref)
+    assert np.array_equal(vis.cpu().numpy(), expected_visited(bits, per_head, B, Hq, Sq, Sk, causal, wl, wr,
+                                                              seqlens_q=lq, seqlens_k=lk))
 
 
 def test_varlen_full_lengths_equal_padded():

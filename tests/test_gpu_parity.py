@@ -10,7 +10,7 @@ import torch
 
 from attention_forward_07_gb300 import inputs as inp
 
-from gpu_util import assert_close, oracle_full, oracle_rows, run_cuda
+from gpu_util import assert_close, expected_visited, oracle_full, oracle_rows, run_cuda
 
 import oracle
 
@@ -95,8 +95,7 @@ def test_skip_map_is_exact(S, causal, mask, d):
     B, H = 2, 3
     q, k, v, bits, causal, scale = _case(B, H, H, S, d, inp.F16, causal, mask, seed=S)
     o, lse, vis = run_cuda(q, k, v, bits, causal, scale, visited=True)
-    ref = oracle.skip_map(bits, B, S, causal, 128, 128)
-    assert np.array_equal(vis, np.repeat(ref[:, None], H, axis=1))
+    assert np.array_equal(vis, expected_visited(bits, False, B, H, S, S, causal))
     o_ref, lse_ref = oracle_full(q, k, v, bits, causal, scale, inp.F16)
     assert_close(o, lse, o_ref, lse_ref, "visited run")
 
@@ -132,8 +131,7 @@ def test_short_workloads_full_parity(name):
     o, lse, vis = run_cuda(q, k, v, bits, w.causal, w.scale, visited=True)
     o_ref, lse_ref = oracle_full(q, k, v, bits, w.causal, w.scale, w.dtype)
     assert_close(o, lse, o_ref, lse_ref, name)
-    ref = oracle.skip_map(bits, w.B, w.S, w.causal, 128, 128)
-    assert np.array_equal(vis, np.repeat(ref[:, None], w.Hq, axis=1))
+    assert np.array_equal(vis, expected_visited(bits, False, w.B, w.Hq, w.S, w.S, w.causal))
 
 
 @pytest.mark.parametrize("name", PREFILL)

@@ -163,3 +163,26 @@ def test_varlen_short_keys_make_early_rows_empty_under_causal():
     tail = oracle.attn_rows_ex(_u16(q[:, :, 4:10].contiguous()), _u16(k[:, :, :6].contiguous()),
                                _u16(v[:, :, :6].contiguous()), inp.F16, None, None, False, True, -1, -1, 0.5)
     assert np.array_equal(o[:, :, 4:10], tail[0]) and np.array_equal(lse[:, :, 4:10], tail[1])
+
+
+def test_expected_visited_compaction_helper():
+    """The helper that states the kernel's visited map under custom masks: with no empty
+    16-row block it is the plain (128, 128) block map; with empty blocks it is built over
+    the compacted rows (live blocks in ascending order, eight per tile)."""
+    from gpu_util import expected_visited
+    B, Hq, S = 2, 3, 300
+    bits = inp.pack_bits(inp.bernoulli_mask(B, S, 5))
+    got = expected_visited(bits, False, B, Hq, S, S, True)
+    ref = oracle.skip_map(bits, B, S, True, 128, 128)
+    assert np.array_equal(got, np.repeat(ref[:, None], Hq, axis=1))
+    keep = np.zeros((1, S, S), bool)
+    keep[0, 2 * 16 + 3, 10] = True     # block 2 -> key tile 0
+    keep[0, 5 * 16 + 9, 200] = True    # block 5 -> key tile 1
+    keep[0, 17 * 16 + 1, 290] = True   # block 17 -> key tile 2
+    bits = inp.pack_bits(keep)
+    got = expected_visited(bits, False, 1, 1, S, S, False)
+    want = np.zeros((1, 1, 3, 3), np.uint8)
+    want[0, 0, 0] = 1                  # all three live blocks land in compacted tile 0
+    assert np.array_equal(got, want)
+    plain = oracle.skip_map(bits, 1, S, False, 128, 128)
+    assert plain[0, 0].tolist() == [1, 1, 0] and plain[0, 2].tolist() == [0, 0, 1]
