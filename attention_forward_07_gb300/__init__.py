@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_ex,
     attn_fwd_noalloc,
+    attn_fwd_packed,
     attn_fwd_visited,
     attn_strerror,
     attn_tile_shape,

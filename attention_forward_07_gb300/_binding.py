@@ -43,7 +43,8 @@ class FwdParams(ctypes.Structure):
                 ("Sk", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int), ("window_left", ctypes.c_int),
                 ("window_right", ctypes.c_int), ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
                 ("stream", ctypes.c_void_p), ("visited", ctypes.c_void_p), ("seqlens_q", ctypes.c_void_p),
-                ("seqlens_k", ctypes.c_void_p)]
+                ("seqlens_k", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+                ("max_seqlen_q", ctypes.c_int), ("max_seqlen_k", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -182,6 +183,29 @@ def attn_fwd_ex(q, k, v, o, lse=None, mask_bits=None, mask_per_head=False, causa
                     visited=None if visited is None else visited.data_ptr(),
                     seqlens_q=None if seqlens_q is None else _lens_ptr(seqlens_q, B),
                     seqlens_k=None if seqlens_k is None else _lens_ptr(seqlens_k, B))
+    rc = library().attn_fwd_ex(ctypes.byref(prm))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_ex")
+
+
+def attn_fwd_packed(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, lse=None, causal=False,
+                    window_left=-1, window_right=-1, scale=None, visited=None, stream=None):
+    """attn_fwd_ex over packed variable-length batches: q/o [Hq, total_q, d], k/v [Hkv, total_k, d],
+    lse [Hq, total_q]; cu_seqlens_q / cu_seqlens_k int32 device tensors [B+1] of row offsets;
+    max_seqlen_q / max_seqlen_k bound the entries' lengths.  See include/attn.h."""
+    Hq, Sq, d = q.shape
+    Hkv, Sk = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    prm = FwdParams(q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), o=o.data_ptr(),
+                    lse=None if lse is None else lse.data_ptr(), mask_bits=None, mask_per_head=0,
+                    B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=d, causal=int(bool(causal)),
+                    window_left=int(window_left), window_right=int(window_right), scale=float(scale),
+                    dtype=_dtype_code(q), stream=_stream_handle(stream).value,
+                    visited=None if visited is None else visited.data_ptr(),
+                    cu_seqlens_q=_lens_ptr(cu_seqlens_q, B + 1), cu_seqlens_k=_lens_ptr(cu_seqlens_k, B + 1),
+                    max_seqlen_q=int(max_seqlen_q), max_seqlen_k=int(max_seqlen_k))
     rc = library().attn_fwd_ex(ctypes.byref(prm))
     if rc != 0:
         raise AttnError(rc, "attn_fwd_ex")

@@ -103,7 +103,7 @@ struct Layout {
   static constexpr int OFF_WORDS = OFF_STAGE + STAGE_BYTES;
   static constexpr int WORDS_PER_ENTRY = UNIT_ROWS * (BN / 32);
   static constexpr int OFF_HDR = OFF_WORDS + (MODE == MASK_CUSTOM ? NINFO * WORDS_PER_ENTRY * 4 : 0);
-  static constexpr int OFF_BAR = OFF_HDR + NINFO * 16;
+  static constexpr int OFF_BAR = OFF_HDR + NINFO * 32;
   // barrier indices
   static constexpr int B_QFULL = 0, B_QEMPTY = QBUF, B_KFULL = 2 * QBUF,
                        B_KEMPTY = B_KFULL + KSLOT, B_VFULL = B_KEMPTY + KSLOT,
@@ -124,7 +124,10 @@ struct InfoHdr {
   int j;      // key tile index
   int flags;  // bit t: Q tile t computes this key tile; FLAG_END: end of unit
   int sq, sk;  // the unit's query and key lengths (per batch entry with seqlens arrays)
+  int qoff;    // packed layouts: the entry's first row in q / o / lse
+  int pad[3];
 };
+static_assert(sizeof(InfoHdr) == 32, "descriptor slot size");
 
 struct Params {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps {d, S, B*H}, box {64, 128, 1}, 128B swizzle
@@ -150,6 +153,12 @@ struct Params {
   int mask_heads;  // custom-mask rows per batch entry: Hq (per-head masks) or 1
   const int* lens_q;  // per batch entry query / key lengths inside the padded buffers,
   const int* lens_k;  // clamped to [0, Sq] / [0, Sk]; NULL = Sq / Sk
+  // Packed layouts (cu_q != NULL): entry b holds rows cu_q[b] .. cu_q[b+1]-1 of q / o / lse
+  // ([Hq][q_rows][d]) and keys cu_k[b] .. cu_k[b+1]-1 of k / v ([Hkv][k_rows][d]); Sq / Sk
+  // are then the longest entry's lengths.
+  const int* cu_q;
+  const int* cu_k;
+  int q_rows, k_rows;
   int causal;      // the band only bounds keys on the right: longest units first
   int inject;
   float scale_log2;
@@ -229,7 +238,25 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
   }
 }
 
-// Query / key lengths of batch entry b (off = sk - sq is its bottom-right alignment).
+// Query / key lengths of batch entry b and, for packed layouts, its first query and key row
+// (off = sk - sq is its bottom-right alignment).
+__device__ __forceinline__ void unit_span(const Params& p, int b, int& sq, int& sk, int& qoff, int& koff) {
+  if (p.cu_q) {
+    qoff = __ldg(p.cu_q + b);
+    koff = __ldg(p.cu_k + b);
+    sq = min(max(__ldg(p.cu_q + b + 1) - qoff, 0), p.Sq);
+    sk = min(max(__ldg(p.cu_k + b + 1) - koff, 0), p.Sk);
+  } else {
+    qoff = koff = 0;
+    sq = p.lens_q ? min(max(__ldg(p.lens_q + b), 0), p.Sq) : p.Sq;
+    sk = p.lens_k ? min(max(__ldg(p.lens_k + b), 0), p.Sk) : p.Sk;
+  }
+}
+// Rows of (b, hq) in q / o / lse start here (padded: its own [Sq] block; packed: the entry's
+// rows inside head hq's [q_rows] block).
+__device__ __forceinline__ size_t q_row_base(const Params& p, int b, int hq, int qoff) {
+  return p.cu_q ? (size_t)hq * p.q_rows + qoff : (size_t)(b * p.Hq + hq) * p.Sq;
+}
 __device__ __forceinline__ void unit_lengths(const Params& p, int b, int& sq, int& sk) {
   sq = p.lens_q ? min(max(__ldg(p.lens_q + b), 0), p.Sq) : p.Sq;
   sk = p.lens_k ? min(max(__ldg(p.lens_k + b), 0), p.Sk) : p.Sk;
@@ -300,6 +327,10 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       in_place = __all_sync(0xffffffffu, lane >= 2 * QT * 4 || slot_blk == (own < p.nr16 ? own : -1));
     }
 
+    int sq, sk, qoff, koff;
+    unit_span(p, b, sq, sk, qoff, koff);
+    const int qz = p.cu_q ? hq : b * p.Hq + hq, kz = p.cu_q ? hkv : b * p.Hkv + hkv;  // TMA z
+
     // Both Q tiles of the unit (rows past S are zero-filled by the TMA unit).  Custom masks
     // gather them block by block from the compacted list (a missing block reads as zeros).
     const int qbuf = k % L::QBUF;
@@ -326,7 +357,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
 #pragma unroll
           for (int h = 0; h < L::HALVES; ++h)
             tma_load_3d(base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES + h * BM * 128,
-                        &p.tm_q, fb, h * 64, row0 + t * BM, b * p.Hq + hq);
+                        &p.tm_q, fb, h * 64, qoff + row0 + t * BM, qz);
       }
       // this fill completes the phase the consumer waits for with parity (empty parity ^ 1)
       q_pend |= 1u << qbuf;
@@ -334,8 +365,6 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     }
     inject = false;
 
-    int sq, sk;
-    unit_lengths(p, b, sq, sk);
     const int off = sk - sq;
     // Key-tile range of each Q tile under the band.  key_lo / key_hi grow by one per row,
     // so the kept keys of rows rf..r1 form the one range [key_lo(rf), key_hi(r1)), rf being
@@ -388,6 +417,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
         hdr[ie].flags = (a0 ? 1 : 0) | (a1 ? 2 : 0);
         hdr[ie].sq = sq;
         hdr[ie].sk = sk;
+        hdr[ie].qoff = qoff;
         const uint32_t fb = bars + 8u * (L::B_IFULL + ie);
         if constexpr (MODE == MASK_CUSTOM) {
           mbar_expect_tx(fb, L::WORDS_PER_ENTRY * 4);
@@ -422,7 +452,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
 #pragma unroll
         for (int h = 0; h < L::HALVES; ++h)
           tma_load_3d(base + L::OFF_K + kslot * L::KV_TILE_BYTES + h * BN * 128, &p.tm_k, fb,
-                      h * 64, j * BN, b * p.Hkv + hkv);
+                      h * 64, koff + j * BN, kz);
       }
       kpend |= 1u << kslot;
       kpend_par = (kpend_par & ~(1u << kslot)) | ((kpar ^ 1u) << kslot);
@@ -435,7 +465,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
 #pragma unroll
         for (int h = 0; h < L::HALVES; ++h)
           tma_load_3d(base + L::OFF_V + vslot * L::KV_TILE_BYTES + h * BN * 128, &p.tm_v, fb,
-                      h * 64, j * BN, b * p.Hkv + hkv);
+                      h * 64, koff + j * BN, kz);
       }
       vpend |= 1u << vslot;
       vpend_par = (vpend_par & ~(1u << vslot)) | ((vpar ^ 1u) << vslot);
@@ -448,6 +478,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       hdr[ie].flags = FLAG_END;
       hdr[ie].sq = sq;
       hdr[ie].sk = sk;
+      hdr[ie].qoff = qoff;
       mbar_arrive(bars + 8u * (L::B_IFULL + ie));
     }
     __syncwarp();
@@ -640,7 +671,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     }
     float m = -INFINITY, l = 0.f;
     int nact = 0;
-    int sq = p.Sq, sk = p.Sk;  // the unit's lengths, carried by every tile descriptor
+    int sq = p.Sq, sk = p.Sk, qoff = 0;  // the unit's lengths and first row, in every descriptor
 
     while (true) {
       if (!bwait_warp(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) return;
@@ -648,6 +679,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       const int flags = hdr[ie].flags;
       sq = hdr[ie].sq;
       sk = hdr[ie].sk;
+      qoff = hdr[ie].qoff;
       const bool end = (flags & FLAG_END) != 0;
       const bool act = !end && ((flags >> t) & 1);
       uint4 wv = make_uint4(0u, 0u, 0u, 0u);
@@ -806,7 +838,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       }
       __syncwarp();
       const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;  // this warp's first row
-      uint8_t* obh = reinterpret_cast<uint8_t*>(p.o) + (size_t)(b * p.Hq + hq) * p.Sq * ROW_BYTES;
+      uint8_t* obh = reinterpret_cast<uint8_t*>(p.o) + q_row_base(p, b, hq, qoff) * ROW_BYTES;
       constexpr int ROWS_PER_STORE = 32 / CHUNKS;
 #pragma unroll
       for (int kk = 0; kk < 32 / ROWS_PER_STORE; ++kk) {
@@ -827,7 +859,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       // each store instruction then writes four whole 128-byte segments of O.
       uint8_t* stage = gbase + L::OFF_STAGE + (t * 4 + quarter) * (32 * 128);
       const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;
-      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + row0w) * (D * 2);
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (q_row_base(p, b, hq, qoff) + row0w) * (D * 2);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
 #pragma unroll
@@ -860,7 +892,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
         __syncwarp();  // the slice is rewritten by the next half
       }
     } else {
-    OutT* orow = reinterpret_cast<OutT*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + (row_ok ? i : 0)) * D;
+    OutT* orow = reinterpret_cast<OutT*>(p.o) + (q_row_base(p, b, hq, qoff) + (row_ok ? i : 0)) * D;
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch) {
       uint32_t ob[16];
@@ -883,7 +915,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     if (L::STAGE_O && lane == 0) mbar_arrive(bars + 8u * (L::B_QEMPTY + (k % L::QBUF)));
     }
     if (row_ok && p.lse)
-      p.lse[(size_t)(b * p.Hq + hq) * p.Sq + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+      p.lse[q_row_base(p, b, hq, qoff) + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
     if constexpr (MODE == MASK_CUSTOM) {
       // The unit also owns the 16-row blocks of its original rows; those with nothing kept
       // were left out of the compacted list: O = 0 and LSE = -inf there, this warp's two
@@ -1327,7 +1359,12 @@ int noalloc_scratch_address(void** out) {
 int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // ---- validation (no CUDA call before this block is passed)
   if (!a.q || !a.k || !a.v || !a.o) return ATTN_ERR_INVALID;
-  if (a.B < 1 || a.Hq < 1 || a.Hkv < 1 || a.Sq < 1 || a.Sk < a.Sq || a.Hq % a.Hkv != 0)
+  const bool packed = a.cu_seqlens_q != nullptr;
+  if (packed != (a.cu_seqlens_k != nullptr)) return ATTN_ERR_INVALID;
+  if (packed && (a.seqlens_q || a.seqlens_k || a.max_seqlen_q < 1 || a.max_seqlen_k < 1)) return ATTN_ERR_INVALID;
+  if (packed && a.mask_bits) return ATTN_ERR_UNSUPPORTED;
+  if (a.B < 1 || a.Hq < 1 || a.Hkv < 1 || a.Sq < 1 || a.Sk < 1 || (!packed && a.Sk < a.Sq) ||
+      a.Hq % a.Hkv != 0)
     return ATTN_ERR_INVALID;
   if (a.window_left < -1 || a.window_right < -1) return ATTN_ERR_INVALID;
   if (a.mask_per_head != 0 && a.mask_per_head != 1) return ATTN_ERR_INVALID;
@@ -1337,10 +1374,13 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   const uintptr_t a16 = (uintptr_t)a.q | (uintptr_t)a.k | (uintptr_t)a.v | (uintptr_t)a.o;
   if (a16 & 15u) return ATTN_ERR_INVALID;
   if (((uintptr_t)a.lse & 3u) || ((uintptr_t)a.mask_bits & 3u) || ((uintptr_t)a.seqlens_q & 3u) ||
-      ((uintptr_t)a.seqlens_k & 3u))
+      ((uintptr_t)a.seqlens_k & 3u) || ((uintptr_t)a.cu_seqlens_q & 3u) || ((uintptr_t)a.cu_seqlens_k & 3u))
     return ATTN_ERR_INVALID;
-  const long long nqb = (a.Sq + UNIT_ROWS - 1) / UNIT_ROWS;
-  if ((long long)a.B * a.Hq * a.Sk > INT_MAX || (long long)a.B * a.Hq * nqb > INT_MAX)
+  // the per-entry extents the kernel works with (packed: the longest entry's)
+  const int Sq = packed ? a.max_seqlen_q : a.Sq, Sk = packed ? a.max_seqlen_k : a.Sk;
+  const long long nqb = (Sq + UNIT_ROWS - 1) / UNIT_ROWS;
+  if ((long long)a.B * a.Hq * Sk > INT_MAX || (long long)a.B * a.Hq * nqb > INT_MAX ||
+      (long long)a.Hq * a.Sq > INT_MAX || (long long)a.Hkv * a.Sk > INT_MAX)
     return ATTN_ERR_INVALID;
 
   int sms = 0, dev = 0;
@@ -1350,9 +1390,11 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   Params p;
   std::memset(&p, 0, sizeof p);
   const bool bf16 = a.dtype == ATTN_BF16;
-  if ((rc = make_map(&p.tm_q, a.q, bf16, a.d, a.Sq, (long long)a.B * a.Hq)) != ATTN_OK) return rc;
-  if ((rc = make_map(&p.tm_k, a.k, bf16, a.d, a.Sk, (long long)a.B * a.Hkv)) != ATTN_OK) return rc;
-  if ((rc = make_map(&p.tm_v, a.v, bf16, a.d, a.Sk, (long long)a.B * a.Hkv)) != ATTN_OK) return rc;
+  // padded: {d, Sq, B*Hq}; packed: {d, total rows, Hq} (an entry's rows at its offset)
+  const long long qz = packed ? a.Hq : (long long)a.B * a.Hq, kz = packed ? a.Hkv : (long long)a.B * a.Hkv;
+  if ((rc = make_map(&p.tm_q, a.q, bf16, a.d, a.Sq, qz)) != ATTN_OK) return rc;
+  if ((rc = make_map(&p.tm_k, a.k, bf16, a.d, a.Sk, kz)) != ATTN_OK) return rc;
+  if ((rc = make_map(&p.tm_v, a.v, bf16, a.d, a.Sk, kz)) != ATTN_OK) return rc;
   if (a.mask_bits && (rc = make_map(&p.tm_q16, a.q, bf16, a.d, a.Sq, (long long)a.B * a.Hq, 16)) != ATTN_OK)
     return rc;
   p.o = a.o;
@@ -1361,14 +1403,18 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
-  p.Sq = a.Sq;
-  p.Sk = a.Sk;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.cu_q = a.cu_seqlens_q;
+  p.cu_k = a.cu_seqlens_k;
+  p.q_rows = a.Sq;
+  p.k_rows = a.Sk;
   p.g = a.Hq / a.Hkv;
   p.nqb = (int)nqb;
-  p.nkt = (a.Sk + BN - 1) / BN;
-  p.nqt = (a.Sq + BM - 1) / BM;
-  p.nr16 = (a.Sq + 15) / 16;
-  p.W = (a.Sk + 31) / 32;
+  p.nkt = (Sk + BN - 1) / BN;
+  p.nqt = (Sq + BM - 1) / BM;
+  p.nr16 = (Sq + 15) / 16;
+  p.W = (Sk + 31) / 32;
   p.num_units = a.B * a.Hq * (int)nqb;
   p.wl = a.window_left;
   p.er = a.causal ? 0 : a.window_right;  // causal: nothing right of the aligned position

@@ -102,9 +102,18 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *     keys j < sk_b exist, and rows i >= sq_b of o and lse are not written.  Key rows at or
  *     past sk_b get weight exactly 0, so v must hold finite values there (0 * inf is NaN);
  *     k there may hold anything.  The custom-mask layout keeps the padded shape.
+ *   - packed variable-length batches: cu_seqlens_q / cu_seqlens_k, int32 [B+1] in device
+ *     memory (4-byte aligned, non-decreasing, cu[0] = 0), or NULL.  When given, entry b is
+ *     query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] ..
+ *     cu_seqlens_k[b+1]-1 of head-major packed buffers: q, o: [Hq][Sq][d], k, v:
+ *     [Hkv][Sk][d], lse: [Hq][Sq], with Sq / Sk the total row counts; max_seqlen_q /
+ *     max_seqlen_k (>= 1) bound every entry's lengths (longer entries are cut to them).
+ *     Alignment, causal and window rules are per entry as above; visited is
+ *     [B][Hq][ceil(max_seqlen_q/bm)][ceil(max_seqlen_k/bn)].  Custom masks are not supported
+ *     with packed layouts (ATTN_ERR_UNSUPPORTED); seqlens_q / seqlens_k must then be NULL.
  * With Sq = Sk = S, windows -1, mask_per_head = 0 and no lengths it is attn_fwd.  Custom masks take
  * stream-ordered scratch of the custom-mask scratch size above.  Errors as for attn_fwd;
- * Sk < Sq is ATTN_ERR_INVALID.
+ * Sk < Sq is ATTN_ERR_INVALID for padded layouts.
  */
 typedef struct {
     const void *q, *k, *v;
@@ -119,6 +128,8 @@ typedef struct {
     void *stream;
     uint8_t *visited;
     const int *seqlens_q, *seqlens_k;
+    const int *cu_seqlens_q, *cu_seqlens_k;
+    int max_seqlen_q, max_seqlen_k;
 } attn_fwd_params_t;
 
 int attn_fwd_ex(const attn_fwd_params_t *params);

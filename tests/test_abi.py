@@ -104,6 +104,12 @@ def test_fwd_ex_validation(lib):
                 window_right=-1, scale=0.125, dtype=0)
     for kw, status in ((dict(Sk=64), -1), (dict(window_left=-2), -1), (dict(window_right=-5), -1),
                        (dict(mask_per_head=2), -1), (dict(d=80), -2), (dict(Sq=0), -1),
-                       (dict(seqlens_q=P + 2), -1), (dict(seqlens_k=P + 1), -1)):
+                       (dict(seqlens_q=P + 2), -1), (dict(seqlens_k=P + 1), -1),
+                       # packed layouts: both offset arrays, no padded lengths, no custom mask
+                       (dict(cu_seqlens_q=P, max_seqlen_q=8, max_seqlen_k=8), -1),
+                       (dict(cu_seqlens_q=P, cu_seqlens_k=P, max_seqlen_q=0, max_seqlen_k=8), -1),
+                       (dict(cu_seqlens_q=P, cu_seqlens_k=P, seqlens_q=P, max_seqlen_q=8, max_seqlen_k=8), -1),
+                       (dict(cu_seqlens_q=P, cu_seqlens_k=P, mask_bits=P, max_seqlen_q=8, max_seqlen_k=8), -2),
+                       (dict(cu_seqlens_q=P + 2, cu_seqlens_k=P, max_seqlen_q=8, max_seqlen_k=8), -1)):
         args = dict(base, **kw)
         assert lib.attn_fwd_ex(ctypes.byref(FwdParams(**args))) == status, kw

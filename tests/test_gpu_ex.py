@@ -173,3 +173,63 @@ def test_varlen_full_lengths_equal_padded():
         af.attn_check()
         outs.append((o.cpu(), lse.cpu()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+PACKED_CASES = [
+    # Hq, Hkv, d, dtype, causal, wl, wr, query lengths, key lengths
+    (4, 2, 128, inp.BF16, True, -1, -1, [300, 0, 129, 512], [300, 77, 400, 512]),
+    (2, 2, 64, inp.F16, False, -1, -1, [1, 256, 333], [700, 256, 333]),
+    (4, 1, 64, inp.F16, True, 100, -1, [200, 450, 17, 256, 90], [200, 900, 17, 300, 1]),
+]
+
+
+@pytest.mark.parametrize("case", PACKED_CASES, ids=lambda c: "Hq{}_Hkv{}_d{}_c{}_w{}_{}_n{}".format(
+    c[0], c[1], c[2], int(c[4]), c[5], c[6], len(c[7])))
+def test_packed_varlen_matches_padded_and_oracle(case):
+    """Packed variable-length batches (cu_seqlens): each entry's rows equal the padded
+    per-entry-length run bit for bit (same tiles, same order) and the oracle within the
+    tolerance; the visited maps agree; rows outside every entry are not written."""
+    Hq, Hkv, d, dtype, causal, wl, wr, lq, lk = case
+    B = len(lq)
+    Sq, Sk = max(lq), max(lk)
+    q, k, v = inp.qkv(B, Hq, Hkv, max(Sq, Sk), d, dtype, 31 * Sq + Sk)
+    q, k, v = q[:, :, :Sq].contiguous(), k[:, :, :Sk].contiguous(), v[:, :, :Sk].contiguous()
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    # head-major packed buffers with two spare rows after the last entry
+    qp = torch.cat([q[b, :, :lq[b]] for b in range(B)] + [torch.zeros(Hq, 2, d, dtype=q.dtype)], dim=1).contiguous()
+    kp = torch.cat([k[b, :, :lk[b]] for b in range(B)] + [torch.zeros(Hkv, 2, d, dtype=k.dtype)], dim=1).contiguous()
+    vp = torch.cat([v[b, :, :lk[b]] for b in range(B)] + [torch.zeros(Hkv, 2, d, dtype=v.dtype)], dim=1).contiguous()
+    dev = "cuda"
+    scale = 1.0 / d ** 0.5
+    o = torch.full((Hq, qp.shape[1], d), float("nan"), dtype=q.dtype, device=dev)
+    lse = torch.full((Hq, qp.shape[1]), float("nan"), dtype=torch.float32, device=dev)
+    vis = torch.zeros((B, Hq, -(-Sq // 128), -(-Sk // 128)), dtype=torch.uint8, device=dev)
+    af.attn_fwd_packed(qp.to(dev), kp.to(dev), vp.to(dev), o, torch.from_numpy(cq).to(dev),
+                       torch.from_numpy(ck).to(dev), Sq, Sk, lse=lse, causal=causal, window_left=wl,
+                       window_right=wr, scale=scale, visited=vis)
+    af.attn_check()
+    # the same batch in padded form with per-entry lengths
+    o2 = torch.full((B, Hq, Sq, d), float("nan"), dtype=q.dtype, device=dev)
+    lse2 = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device=dev)
+    vis2 = torch.zeros_like(vis)
+    lqt = torch.tensor(lq, dtype=torch.int32, device=dev)
+    lkt = torch.tensor(lk, dtype=torch.int32, device=dev)
+    if Sk < Sq:
+        pytest.skip("padded form needs Sk >= Sq")
+    af.attn_fwd_ex(q.to(dev), k.to(dev), v.to(dev), o2, lse2, None, False, causal, wl, wr, scale, vis2,
+                   seqlens_q=lqt, seqlens_k=lkt)
+    af.attn_check()
+    o, lse, o2, lse2 = o.cpu(), lse.cpu(), o2.cpu(), lse2.cpu()
+    assert torch.all(torch.isnan(o[:, cq[-1]:])) and torch.all(torch.isnan(lse[:, cq[-1]:]))
+    o_ref, lse_ref = oracle.attn_rows_ex(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), dtype, None, None, False,
+                                         causal, wl, wr, float(np.float32(scale)), seqlens_q=np.array(lq),
+                                         seqlens_k=np.array(lk))
+    for b in range(B):
+        rows = slice(int(cq[b]), int(cq[b + 1]))
+        n = lq[b]
+        assert torch.equal(o[:, rows], o2[b, :, :n]) and torch.equal(lse[:, rows], lse2[b, :, :n]), f"entry {b}"
+        if n:
+            assert_close(o[:, rows].float().numpy().astype(np.float64), lse[:, rows].numpy().astype(np.float64),
+                         o_ref[b, :, :n], lse_ref[b, :, :n], f"{case} entry {b}")
+    assert torch.equal(vis.cpu(), vis2.cpu())
