@@ -203,6 +203,18 @@ def cpu_baseline(w, seed, target_seconds: float):
     return flops / dt / 1e12, oracle.num_threads(), f"{n} random rows of {total_rows} (seeded), fp64", dt
 
 
+def cpu_single_thread(w, seed):
+    """The whole oracle on one host thread (small workloads only), TFLOPS-equivalent."""
+    import oracle
+    from attention_forward_07_gb300 import inputs as inp
+    q, k, v, bits = w.make(seed)
+    rows = np.arange(w.B * w.Hq * w.S, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attn_rows(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), w.dtype, rows, bits, w.causal, w.scale,
+                     nthreads=1)
+    return w.flops() / (time.perf_counter() - t0) / 1e12
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -363,6 +375,8 @@ def run_ours(args):
         tf, cores, sample, secs = cpu_baseline(w, seed, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample,
                                 "seconds": secs}
+        if w.B * w.Hq * w.S <= 4096:  # the tiny workload: also the whole oracle on one thread
+            line["cpu_baseline"]["single_thread_value"] = cpu_single_thread(w, seed)
     else:
         line["cpu_baseline"] = None
     if rank == 0:
