@@ -256,12 +256,12 @@ def run_reference(args):
 # keyed by the sha1 of the kernel sources they were taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, per kernel
-    # source hash.  Causal GQA B=2 S=4096 was captured (131.89 MB); the default B=4 S=8192
+    # source hash.  Causal GQA B=2 S=4096 was captured (132.05 MB); the default B=4 S=8192
     # launch processes 4x the units and reads 4x the compulsory Q/K/V bytes, so its traffic
-    # is scaled by 4.  The short masked workload was captured at full size (50.97 MB).
-    "8d7a5a9a5887": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 4 * 131.89e6,
-                     "B2_Hq32_Hkv8_S4096_d128_causal_none": 131.89e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.97e6},
+    # is scaled by 4.  The short masked workload was captured at full size (50.95 MB).
+    "40897ef26915": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 4 * 132.05e6,
+                     "B2_Hq32_Hkv8_S4096_d128_causal_none": 132.05e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.95e6},
 }
 
 
