@@ -393,8 +393,8 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       bool a0 = j >= jlo[0] && j <= jhi[0];
       bool a1 = j >= jlo[1] && j <= jhi[1];
       if constexpr (MODE == MASK_CUSTOM) {
-        // Emptiness bits of the two Q tiles for 32 key tiles at a time, from the map the
-        // mask pre-pass wrote (exact: custom bits AND causal AND key bound).
+        // Emptiness bits of the two compacted Q tiles for 32 key tiles at a time, from the
+        // map the mask kernels wrote (exact: custom bits AND band AND lengths).
         if (j == jbeg || (j & 31) == 0) {
           const int jj = (j & ~31) + lane;
           const size_t fb = ((size_t)mb * p.nqt + qb * QT) * p.nkt;
@@ -990,8 +990,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Custom masks: the set-up above overlapped the mask pre-pass (dependent launch); its
-  // words and block flags are read only after this point.
+  // Custom masks: the set-up above overlapped the mask kernels (dependent launch); their
+  // words, flags and slot lists are read only after this point.
   if constexpr (MODE == MASK_CUSTOM) grid_dependency_wait();
 
   // Register rebalancing: the load / MMA warpgroup (warps 0-3) needs few registers, the
@@ -1222,9 +1222,7 @@ int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nm
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Scratch of the custom-mask pre-pass for nmb mask row blocks (B, or B*Hq for per-head
-// masks): padded kept-bit words [nmb][Sq][W4] then the block emptiness flags
-// [nmb][nqt][nkt].
+// Scratch of the custom-mask kernels for nmb mask row blocks (B, or B*Hq for per-head masks).
 struct MaskScratch {
   // kept-bit words [nmb][Sq][W4], flags per (16-row block, key tile) [nmb][nr16][nkt],
   // live 16-row blocks [nmb][nr16], compacted slot -> block [nmb][nqb * 16] (int, 16 slots per
@@ -1306,7 +1304,7 @@ int launch(const Params& p, int grid, cudaStream_t st, int dev) {
     attr_set.fetch_or(bit);
   }
   if constexpr (MODE == MASK_CUSTOM) {
-    // Launched as a programmatic dependent of the mask pre-pass just enqueued on `st`.
+    // Launched as a programmatic dependent of the mask compaction just enqueued on `st`.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(NTHREADS);

@@ -259,19 +259,26 @@ MEASURED_TRAFFIC = {
     # source hash.  Causal GQA B=2 S=4096 was captured (132.05 MB); the default B=4 S=8192
     # launch processes 4x the units and reads 4x the compulsory Q/K/V bytes, so its traffic
     # is scaled by 4.  The short masked workload was captured at full size (50.95 MB).
-    "40897ef26915": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 4 * 132.05e6,
+    "11ae5e36e185": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 4 * 132.05e6,
                      "B2_Hq32_Hkv8_S4096_d128_causal_none": 132.05e6,
                      "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.95e6},
 }
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel sources with comments and blank lines removed, so that the measured
+    figures keyed by it stay attached to the code they were taken on."""
     import hashlib
+    import re
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "attention_forward_07_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(name.encode() + text.encode())
     return h.hexdigest()[:12]
 
 
