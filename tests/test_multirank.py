@@ -49,3 +49,25 @@ def test_single_rank_defaults():
     assert bench.dist_env()[0] == 1
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.replica_seed(7, 0) == 7
+
+
+def test_bench_helpers_without_a_gpu():
+    """The parts of the benchmark line that need no GPU: kernel counting per step, the
+    comment-insensitive kernel hash, the roofline bound choice and the measured-traffic key."""
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from attention_forward_07_gb300 import inputs as inp
+    assert bench.kernels_per_step(inp.WORKLOADS["short_masked"]) == 3
+    assert bench.kernels_per_step(inp.WORKLOADS["gqa8_causal_S8192"]) == 1
+    h = bench.kernel_hash()
+    assert len(h) == 12 and h == bench.kernel_hash()
+    w = inp.WORKLOADS["gqa8_causal_S8192"]
+    r = bench.roofline(w, 1.4e-3)
+    assert r["bound"] == "tensor" and abs(r["achieved"] - w.flops() / 1.4e-3 / 1e12) < 1e-6
+    assert bench.config_key(w) == "B4_Hq32_Hkv8_S8192_d128_causal_none"
+    r = bench.roofline(inp.WORKLOADS["short_masked"], 60e-6)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
