@@ -18,8 +18,10 @@ from ._binding import (  # noqa: F401
     attn_fwd_noalloc,
     attn_fwd_packed,
     attn_fwd_visited,
+    attn_release_workspace,
     attn_strerror,
     attn_tile_shape,
+    debug_counters,
     library,
     library_path,
 )

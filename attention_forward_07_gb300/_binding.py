@@ -27,6 +27,8 @@ EXPORTS = (
     "attn_fwd_noalloc",
     "attn_fwd_ex",
     "attn_check",
+    "attn_release_workspace",
+    "attn_debug_counters",
     "attn_strerror",
     "attn_tile_shape",
     "attn_set_wait_timeout_ns",
@@ -81,6 +83,10 @@ def library():
         lib.attn_fwd_ex.restype = i
         lib.attn_check.argtypes = [p]
         lib.attn_check.restype = i
+        lib.attn_release_workspace.argtypes = [p]
+        lib.attn_release_workspace.restype = i
+        lib.attn_debug_counters.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i]
+        lib.attn_debug_counters.restype = i
         lib.attn_strerror.argtypes = [i]
         lib.attn_strerror.restype = ctypes.c_char_p
         lib.attn_tile_shape.argtypes = [i, ctypes.POINTER(i), ctypes.POINTER(i)]
@@ -217,6 +223,22 @@ def attn_check(stream=None) -> int:
     if rc != 0:
         raise AttnError(rc, "attn_check")
     return rc
+
+
+def attn_release_workspace(stream=None) -> None:
+    """Free the custom-mask workspace the library holds for `stream` (stream-ordered)."""
+    rc = library().attn_release_workspace(_stream_handle(stream))
+    if rc != 0:
+        raise AttnError(rc, "attn_release_workspace")
+
+
+def debug_counters() -> dict:
+    """Host-side counters: workspace allocations, tensor maps encoded, tensor-map cache hits."""
+    out = (ctypes.c_ulonglong * 3)()
+    rc = library().attn_debug_counters(out, 3)
+    if rc != 0:
+        raise AttnError(rc, "attn_debug_counters")
+    return {"workspace_allocs": out[0], "map_encodes": out[1], "map_hits": out[2]}
 
 
 def attn_tile_shape(d: int):

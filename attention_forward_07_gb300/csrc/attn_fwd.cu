@@ -46,7 +46,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <mutex>
+#include <unordered_map>
 
 #include "attn.h"
 #include "ptx.cuh"
@@ -161,20 +163,24 @@ struct Params {
   int q_rows, k_rows;
   int causal;      // the band only bounds keys on the right: longest units first
   int inject;
+  int status_slot;  // index into g_attn_status of the stream this launch runs on
   float scale_log2;
   uint32_t timeout_us;  // longest barrier wait (microseconds; 32 bits keep it in one register)
 };
 
 }  // namespace attn
 
-// Device status word: bit 0 = a barrier wait ran out of time.
-__device__ unsigned int g_attn_status;
+// Device status words, one per stream slot (the host gives every (device, stream) pair a
+// slot; streams beyond the table share slot 0): bit 0 = a barrier wait ran out of time.
+constexpr int STATUS_SLOTS = 1024;
+__device__ unsigned int g_attn_status[STATUS_SLOTS];
 
 namespace attn {
 
 // Slow path of a bounded barrier wait (inlined: a shared non-inlined callee cannot serve
 // warps running under different setmaxnreg budgets).  Gives up when another thread has aborted, when
-// the wait has lasted timeout_us, or after an iteration cap, and then aborts the CTA.
+// the wait has lasted timeout_us, or after an iteration cap, and then aborts the CTA and marks the
+// launch's status slot (abort_flag[1], set from the launch parameters at kernel start).
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        uint32_t timeout_us) {
   const uint64_t t0 = globaltimer_ns();
@@ -184,7 +190,7 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatil
     if ((it & 15u) == 15u && globaltimer_ns() - t0 > 1000ull * timeout_us) break;
   }
   *abort_flag = 1;
-  atomicOr(&g_attn_status, 1u);
+  atomicOr(&g_attn_status[abort_flag[1] & (STATUS_SLOTS - 1)], 1u);
   return false;
 }
 
@@ -974,7 +980,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bars + 8u * (L::B_ODONE + t), 1);
     }
     mbar_init(bars + 8u * L::B_DRAIN, 1);
-    *abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[1] = p.status_slot;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -1190,9 +1197,61 @@ int device_info(int& sms, int& dev) {
   return ATTN_OK;
 }
 
+// Host-side counters (attn_debug_counters): workspace allocations, tensor-map encodes and
+// tensor-map cache hits since the library was loaded.
+std::atomic<unsigned long long> g_ws_allocs{0}, g_map_encodes{0}, g_map_hits{0};
+
+// Tensor maps cached by (kind, address, dims, box rows): a map holds nothing but these, so a
+// cached map is valid for any later call that names the same buffer with the same shape.
+// Least-recently-used replacement over a small table.
+enum MapKind { MAP_F16 = 0, MAP_BF16 = 1, MAP_WORDS = 2 };
+struct MapKey {
+  int kind;
+  const void* ptr;
+  long long d0, d1, d2;
+  int box_rows;
+  bool operator==(const MapKey& o) const {
+    return kind == o.kind && ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && box_rows == o.box_rows;
+  }
+};
+constexpr int MAP_CACHE = 64;
+struct MapSlot {
+  MapKey key;
+  CUtensorMap map;
+  unsigned long long used = 0;  // 0 = empty
+};
+std::mutex g_map_mutex;
+MapSlot g_maps[MAP_CACHE];
+unsigned long long g_map_clock = 0;
+
+template <class Encode>
+int cached_map(CUtensorMap* m, const MapKey& key, Encode encode) {
+  {
+    std::lock_guard<std::mutex> lk(g_map_mutex);
+    for (MapSlot& e : g_maps)
+      if (e.used && e.key == key) {
+        e.used = ++g_map_clock;
+        *m = e.map;
+        g_map_hits.fetch_add(1);
+        return ATTN_OK;
+      }
+  }
+  const int rc = encode(m);
+  if (rc != ATTN_OK) return rc;
+  g_map_encodes.fetch_add(1);
+  std::lock_guard<std::mutex> lk(g_map_mutex);
+  MapSlot* victim = &g_maps[0];
+  for (MapSlot& e : g_maps)
+    if (e.used < victim->used) victim = &e;
+  victim->key = key;
+  victim->map = *m;
+  victim->used = ++g_map_clock;
+  return ATTN_OK;
+}
+
 // [rows = B*H][S][d] tensor as a 3-D map {d, S, B*H}; box {64, box_rows, 1}: one 128-byte
 // swizzle span of box_rows rows.  Rows past S read as zeros.
-int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long BH, int box_rows = 128) {
+int encode_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long BH, int box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)BH};
@@ -1206,10 +1265,15 @@ int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int S, long long BH, int box_rows = 128) {
+  return cached_map(m, MapKey{bf16 ? MAP_BF16 : MAP_F16, ptr, d, S, BH, box_rows},
+                    [&](CUtensorMap* out) { return encode_map(out, ptr, bf16, d, S, BH, box_rows); });
+}
+
 // Kept-bit words of a custom mask after the pre-pass: 3-D map {W4, S, nmb} of uint32, box
 // {4 words, box_rows, 1}: one key tile's words for one 16-row block (gathered per slot) or
 // for the 256 rows of a unit whose compacted slots are its own rows.
-int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nmb, int box_rows) {
+int encode_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nmb, int box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return ATTN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)W4, (cuuint64_t)Sq, (cuuint64_t)nmb};
@@ -1220,6 +1284,71 @@ int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nm
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int make_mask_map(CUtensorMap* m, const uint32_t* words4, int W4, int Sq, int nmb, int box_rows) {
+  return cached_map(m, MapKey{MAP_WORDS, words4, W4, Sq, nmb, box_rows},
+                    [&](CUtensorMap* out) { return encode_mask_map(out, words4, W4, Sq, nmb, box_rows); });
+}
+
+// ---------------------------------------------------------------- per-stream state
+// Every (device, stream) the library launches on gets a status slot (the index of its word
+// in g_attn_status; slot 0 is shared by the streams beyond the table) and, once it runs a
+// custom mask, a workspace for the mask kernels: a stream-ordered allocation that is reused
+// by every later call on that stream and replaced (the old block freed in stream order) only
+// when a call needs more.  `m` is held while a call enqueues work that uses the workspace, so
+// no call frees a block another call on the same stream has already handed to a kernel.
+struct StreamKey {
+  int dev;
+  void* stream;
+  bool operator==(const StreamKey& o) const { return dev == o.dev && stream == o.stream; }
+};
+struct StreamKeyHash {
+  size_t operator()(const StreamKey& k) const {
+    return std::hash<void*>()(k.stream) ^ (std::hash<int>()(k.dev) * 0x9E3779B97F4A7C15ull);
+  }
+};
+struct StreamState {
+  int slot = 0;
+  std::mutex m;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+std::mutex g_streams_mutex;
+std::unordered_map<StreamKey, std::unique_ptr<StreamState>, StreamKeyHash> g_streams;
+int g_next_slot[64];
+
+// The state of (dev, stream), created on first use when `create`; nullptr if absent.
+StreamState* stream_state(int dev, void* stream, bool create) {
+  std::lock_guard<std::mutex> lk(g_streams_mutex);
+  const StreamKey key{dev, stream};
+  auto it = g_streams.find(key);
+  if (it != g_streams.end()) return it->second.get();
+  if (!create) return nullptr;
+  auto st = std::make_unique<StreamState>();
+  int& next = g_next_slot[dev];
+  if (next == 0) next = 1;
+  st->slot = next < STATUS_SLOTS ? next++ : 0;
+  StreamState* raw = st.get();
+  g_streams.emplace(key, std::move(st));
+  return raw;
+}
+
+// Makes s.ws hold at least `need` bytes (caller holds s.m).  Grows in whole MiB.
+int ensure_workspace(StreamState& s, size_t need, cudaStream_t st) {
+  if (s.ws_bytes >= need) return ATTN_OK;
+  const size_t bytes = (need + (1u << 20) - 1) & ~(size_t)((1u << 20) - 1);
+  if (s.ws) {
+    if (cudaFreeAsync(s.ws, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    s.ws = nullptr;
+    s.ws_bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMallocAsync(&p, bytes, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  g_ws_allocs.fetch_add(1);
+  s.ws = p;
+  s.ws_bytes = bytes;
+  return ATTN_OK;
 }
 
 // Scratch of the custom-mask kernels for nmb mask row blocks (B, or B*Hq for per-head masks).
@@ -1332,25 +1461,17 @@ int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev) {
 }
 
 // ---------------------------------------------------------------- no-allocation variant
-// Scratch for attn_fwd_noalloc: a fixed device array instead of cudaMallocAsync.  In host
-// code the symbol is only a host-side stand-in; its device address comes from
-// cudaGetSymbolAddress, looked up once per device (with that device current) on the
-// first attn_fwd_noalloc call made on it.
+// Scratch for attn_fwd_noalloc: a fixed device array instead of a stream-ordered workspace.
+// In host code the symbol is only a host-side stand-in; its device address comes from
+// cudaGetSymbolAddress, asked for on every call with the caller's device current, so a
+// context that was reset or replaced (the module then reloads, possibly elsewhere) never
+// gets a stale address.  The first call on a device loads the module's device code.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
-std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[64] = {};
 
 int noalloc_scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_DEVICE;
-  std::lock_guard<std::mutex> lk(g_noalloc_mutex);
-  if (!g_noalloc_addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-      return ATTN_ERR_CUDA;
-    g_noalloc_addr[dev] = ptr;
-  }
-  *out = g_noalloc_addr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
+  *out = ptr;
   return ATTN_OK;
 }
 
@@ -1432,30 +1553,30 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
                    : (p.wl < 0 && p.er == 0)           ? MASK_CAUSAL
                                                        : MASK_BAND;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(a.stream);
-  // Custom masks: stream-ordered scratch for the pre-pass output, freed in stream order
-  // after the launch that reads it.
-  void* scratch = nullptr;
-  bool owned = false;
-  if (mode == MASK_CUSTOM) {
-    const size_t need = MaskScratch((long long)a.B * p.mask_heads, a.Sq, a.Sk).total();
-    if (noalloc) {
-      // the fixed array: reject what does not fit before anything is launched
-      if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID;
-      if ((rc = noalloc_scratch_address(&scratch)) != ATTN_OK) return rc;
-    } else {
-      if (cudaMallocAsync(&scratch, need, st) != cudaSuccess) return ATTN_ERR_CUDA;
-      owned = true;
-    }
-    rc = prepare_mask(p, a.mask_bits, scratch, st, dev);
-  }
-  if (rc == ATTN_OK) {
+  // The stream's status slot.  attn_fwd_noalloc allocates nothing, not even the host-side
+  // entry of a stream it has not seen: such a stream reports through the shared slot 0.
+  StreamState* ss = stream_state(dev, a.stream, !noalloc);
+  p.status_slot = ss ? ss->slot : 0;
+  const auto run = [&]() {
     if (a.d == 64)
-      rc = bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
-    else
-      rc = bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
+      return bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
+    return bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
+  };
+  if (mode != MASK_CUSTOM) return run();
+  // Custom masks: the mask kernels write into scratch that the attention kernel reads.
+  const size_t need = MaskScratch((long long)a.B * p.mask_heads, a.Sq, a.Sk).total();
+  if (noalloc) {
+    // the fixed array: reject what does not fit before anything is launched
+    if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID;
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch_address(&scratch)) != ATTN_OK) return rc;
+    if ((rc = prepare_mask(p, a.mask_bits, scratch, st, dev)) != ATTN_OK) return rc;
+    return run();
   }
-  if (owned && cudaFreeAsync(scratch, st) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
-  return rc;
+  std::lock_guard<std::mutex> lk(ss->m);
+  if ((rc = ensure_workspace(*ss, need, st)) != ATTN_OK) return rc;
+  if ((rc = prepare_mask(p, a.mask_bits, ss->ws, st, dev)) != ATTN_OK) return rc;
+  return run();
 }
 
 attn_fwd_params_t square_params(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -1521,16 +1642,46 @@ int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float
 }
 
 int attn_check(void* stream) {
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_DEVICE;
+  const attn::StreamState* ss = attn::stream_state(dev, stream, false);
+  const size_t off = (size_t)(ss ? ss->slot : 0) * sizeof(unsigned int);
+  // The status word is read in stream order, after everything enqueued on `stream` so far.
   unsigned int status = 0;
-  if (cudaMemcpyFromSymbol(&status, g_attn_status, sizeof status) != cudaSuccess)
+  if (cudaMemcpyFromSymbolAsync(&status, g_attn_status, sizeof status, off, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
     return ATTN_ERR_CUDA;
   if (status != 0) {
     const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_attn_status, &zero, sizeof zero, off, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return ATTN_ERR_CUDA;
     return ATTN_ERR_TIMEOUT;
   }
+  return ATTN_OK;
+}
+
+int attn_release_workspace(void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ERR_DEVICE;
+  attn::StreamState* ss = attn::stream_state(dev, stream, false);
+  if (!ss) return ATTN_OK;
+  std::lock_guard<std::mutex> lk(ss->m);
+  if (ss->ws) {
+    if (cudaFreeAsync(ss->ws, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    ss->ws = nullptr;
+    ss->ws_bytes = 0;
+  }
+  return ATTN_OK;
+}
+
+int attn_debug_counters(unsigned long long* out, int n) {
+  if (!out || n < 1) return ATTN_ERR_INVALID;
+  const unsigned long long v[3] = {attn::g_ws_allocs.load(), attn::g_map_encodes.load(), attn::g_map_hits.load()};
+  for (int i = 0; i < n; ++i) out[i] = i < 3 ? v[i] : 0ull;
   return ATTN_OK;
 }
 

@@ -1,18 +1,21 @@
 """Benchmark: fused attention forward on GB300, one JSON line on stdout (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--no-sweep] [--no-cpu-baseline] [--no-e2e] [--no-clocks]
 
 A step is one launch of the fused forward over one batch of the workload (inputs
 resident in HBM).  Default workload: causal GQA prefill, Hq=32, Hkv=8, d=128, bf16,
 S=8192, B=4 (B*S = 32768 tokens) -- the prefill configuration that runs the most of
 the path at once (scheduler with longest-first causal order, causal bit masking and
 tile skipping, GQA head mapping, both tensor-core contractions, online softmax,
-correction, epilogue).  Every other workload of the pages is available through
---workload.
+correction, epilogue).  The line's headline fields are that workload's; its "sweep" key
+times every workload of the pages' benchmarks the same way (10 warm-up launches, the
+median of 50 timed ones), with each one's roofline fraction and, for the custom-mask
+workloads, the number of skipped tiles against the oracle's count.
 
 Under torchrun (--gpus N > 1) every rank runs its own replica of the workload on its
 own GPU (weak scaling, no collective on the data path); the timed region is bracketed
-by barriers and the slowest rank's time is reported.
+by barriers and the slowest rank's time is reported; there is no sweep.
 
 --impl reference times the fp64 CPU oracle (the only reference implementation this
 project has) on a bounded random row sample of the same workload, on rank 0 only.
@@ -41,13 +44,14 @@ def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
     return ap.parse_args(argv)
 
@@ -95,16 +99,34 @@ def workload(name: str, batch: int = 0):
     return w, list(inp.WORKLOADS).index(name)
 
 
-def algorithmic_bytes(w) -> int:
-    """Compulsory HBM traffic of one launch: Q, K, V read once, O and LSE written once,
-    mask words read once."""
+def live_fraction(w, bits) -> float:
+    """Fraction of (batch entry, 16-row block) pairs of a custom mask that keep anything
+    (1.0 without a mask): the query rows the kernel has to read and compute."""
+    if bits is None:
+        return 1.0
+    nz = np.asarray(bits).reshape(w.B, w.S, -1).any(axis=2)  # rows that keep anything
+    pad = (-w.S) % 16
+    if pad:
+        nz = np.concatenate([nz, np.zeros((w.B, pad), bool)], axis=1)
+    return float(nz.reshape(w.B, -1, 16).any(axis=2).mean())
+
+
+def algorithmic_bytes(w, live: float = 1.0) -> int:
+    """Compulsory HBM traffic of one launch: K, V, the mask words and the Q rows of the
+    16-row blocks that keep anything read once, O and LSE written once."""
     el = 2
     q = w.B * w.Hq * w.S * w.d * el
     kv = 2 * w.B * w.Hkv * w.S * w.d * el
     o = q
     lse = w.B * w.Hq * w.S * 4
     mask = w.B * w.S * ((w.S + 31) // 32) * 4 if w.mask != "none" else 0
-    return q + kv + o + lse + mask
+    return int(round(q * live)) + kv + o + lse + mask
+
+
+def algorithmic_flops(w, live: float = 1.0) -> float:
+    """The two contractions over the query rows that keep anything: the dense count
+    4*B*Hq*S^2*d (halved for causal) times the live fraction."""
+    return w.flops() * live
 
 
 def config_dict(w, name, n):
@@ -112,8 +134,12 @@ def config_dict(w, name, n):
             "causal": w.causal, "mask": w.mask,
             "dtype_in": {0: "f16", 1: "bf16"}[w.dtype], "global_batch": w.B * n, "seq_len": w.S,
             "parallelism": f"replicas x{n}" if n > 1 else "single GPU",
-            "l2": ("inputs larger than L2, no flush" if algorithmic_bytes(w) > 2 * L2_BYTES
+            "l2": ("inputs larger than L2, no flush" if needs_flush(w) is False
                    else "L2 flushed (256 MiB write) between timed launches")}
+
+
+def needs_flush(w) -> bool:
+    return algorithmic_bytes(w) <= 2 * L2_BYTES
 
 
 def peaks():
@@ -181,26 +207,38 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- the oracle baseline
 
 def cpu_baseline(w, seed, target_seconds: float):
-    """The fp64 oracle, as it stands, on a bounded random row sample of the workload.
-    Returns (TFLOPS-equivalent, threads, sample description, seconds)."""
+    """The fp64 oracle, as it stands, on the host cores.  The short workloads are evaluated
+    whole.  For the prefill workloads the whole oracle would take hours, so it runs on the
+    row sample the measurement protocol names -- for every (batch, head): rows 0, 1, 127,
+    128, S-1 and 64 seeded random rows -- repeated until about target_seconds have passed,
+    and the whole-workload time is extrapolated from its rows per second.
+    Returns a dict for the JSON line."""
     import oracle
     from attention_forward_07_gb300 import inputs as inp
     q, k, v, bits = w.make(seed)
     total_rows = w.B * w.Hq * w.S
-    rng = np.random.default_rng(seed)
-    # calibrate on a small sample, then size the timed sample to ~target_seconds
-    probe = rng.choice(total_rows, size=min(total_rows, 256), replace=False).astype(np.int64)
     args = (inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), w.dtype)
-    t0 = time.perf_counter()
-    oracle.attn_rows(*args, probe, bits, w.causal, w.scale)
-    rate = len(probe) / max(time.perf_counter() - t0, 1e-6)
-    n = int(min(total_rows, max(256, rate * target_seconds)))
-    rows = np.sort(rng.choice(total_rows, size=n, replace=False)).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.attn_rows(*args, rows, bits, w.causal, w.scale)
-    dt = time.perf_counter() - t0
-    flops = w.flops() * n / total_rows
-    return flops / dt / 1e12, oracle.num_threads(), f"{n} random rows of {total_rows} (seeded), fp64", dt
+    whole = total_rows <= 16 * 16 * 512
+    rows = (np.arange(total_rows, dtype=np.int64) if whole
+            else inp.sample_rows(w.B, w.Hq, w.S, 64, seed=seed))
+    passes, dt = 0, 0.0
+    while passes == 0 or (not whole and dt < target_seconds):
+        t0 = time.perf_counter()
+        oracle.attn_rows(*args, rows, bits, w.causal, w.scale)
+        dt += time.perf_counter() - t0
+        passes += 1
+    per_pass = dt / passes
+    full_seconds = per_pass * total_rows / len(rows)
+    out = {"value": w.flops() / full_seconds / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+           "kind": "oracle", "rows_per_second": len(rows) / per_pass, "seconds": dt}
+    if whole:
+        out["sample"] = f"the whole workload ({total_rows} rows), fp64"
+    else:
+        out["sample"] = (f"{len(rows)} rows of {total_rows} (every (b, hq): rows 0, 1, 127, 128, S-1 and 64 "
+                         f"seeded random rows), fp64, {passes} passes")
+        out["extrapolated"] = True
+        out["extrapolated_seconds"] = full_seconds
+    return out
 
 
 def cpu_single_thread(w, seed):
@@ -282,21 +320,23 @@ def kernel_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def roofline(w, seconds_per_launch):
+def roofline(w, seconds_per_launch, live: float = 1.0):
+    """The slower of the tensor and HBM bounds for the algorithmic FLOP and bytes, and the
+    fraction of it this launch time reaches."""
     p_tensor, p_hbm, src = peaks()
-    flops, nbytes = w.flops(), algorithmic_bytes(w)
+    flops, nbytes = algorithmic_flops(w, live), algorithmic_bytes(w, live)
     t_tensor = flops / (p_tensor * 1e12)
     t_hbm = nbytes / (p_hbm * 1e9)
     traffic = MEASURED_TRAFFIC.get(kernel_hash(), {}).get(config_key(w))
+    common = {"traffic": traffic, "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "live_fraction": live,
+              "roofline_ms": 1e3 * max(t_tensor, t_hbm)}
     if t_tensor >= t_hbm:
         ach = flops / seconds_per_launch / 1e12
         return {"bound": "tensor", "achieved": ach, "peak": p_tensor, "unit": "TFLOP/s", "frac": ach / p_tensor,
-                "traffic": traffic, "peak_source": f"{src} bf16 dense (burst)",
-                "algorithmic_flops": flops, "algorithmic_bytes": nbytes}
+                "peak_source": f"{src} bf16 dense (burst)", **common}
     ach = nbytes / seconds_per_launch / 1e9
     return {"bound": "hbm", "achieved": ach, "peak": p_hbm, "unit": "GB/s", "frac": ach / p_hbm,
-            "traffic": traffic, "peak_source": f"{src} HBM copy", "algorithmic_flops": flops,
-            "algorithmic_bytes": nbytes}
+            "peak_source": f"{src} HBM copy", **common}
 
 
 def kernels_per_step(w) -> int:
@@ -307,6 +347,89 @@ def kernels_per_step(w) -> int:
 
 def config_key(w):
     return f"B{w.B}_Hq{w.Hq}_Hkv{w.Hkv}_S{w.S}_d{w.d}_{'causal' if w.causal else 'full'}_{w.mask}"
+
+
+def device_inputs(torch, dev, w, seed):
+    q, k, v, bits = w.make(seed)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if bits is None else torch.from_numpy(bits.view(np.int32)).to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    return (q, k, v, bits), (qd, kd, vd, md, o, lse)
+
+
+def launch_times(torch, dev, step, warmup, timed, flush_buf):
+    """Per-launch device times (ms) of `timed` launches after `warmup` untimed ones, CUDA
+    events on the launching stream around each launch; the L2 is flushed between launches
+    (by writing flush_buf, outside the events) when a buffer is given."""
+    for _ in range(max(warmup, 0)):
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(timed)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(timed)]
+    torch.cuda.synchronize(dev)
+    for i in range(timed):
+        if flush_buf is not None:
+            flush_buf.fill_(i & 0xFF)
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def skip_counts(af, torch, dev, w, tensors):
+    """Blocks computed and skipped by the kernel (attn_fwd_visited, outside any timing)
+    next to the oracle's counts for the same seeded mask (tests/golden/skip_counts.json,
+    written by tests/golden/make_skip_counts.py)."""
+    import hashlib
+    qd, kd, vd, md, o, lse = tensors
+    bm, bn = af.attn_tile_shape(w.d)
+    vis = torch.zeros((w.B, w.Hq, -(-w.S // bm), -(-w.S // bn)), dtype=torch.uint8, device=dev)
+    af.attn_fwd_visited(qd, kd, vd, o, lse, md, w.causal, w.scale, vis)
+    af.attn_check()
+    computed = int(vis.sum().item())
+    out = {"blocks": vis.numel(), "computed": computed, "skipped": vis.numel() - computed}
+    try:
+        with open(os.path.join(ROOT, "tests", "golden", "skip_counts.json")) as f:
+            ref = json.load(f)[w.name]
+        bits = md.cpu().numpy().view(np.uint32)
+        if ref["mask_sha1"] == hashlib.sha1(bits.tobytes()).hexdigest():
+            out["oracle_skipped"] = ref["skipped"]
+            out["match"] = ref["skipped"] == out["skipped"] and ref["computed"] == computed
+        else:
+            out["oracle_skipped"] = None  # the stored count is for other mask words
+    except (OSError, KeyError):
+        out["oracle_skipped"] = None
+    return out
+
+
+def run_sweep(af, torch, dev, warmup=10, timed=50):
+    """Every workload of the pages' benchmarks, timed like the headline one."""
+    from attention_forward_07_gb300 import inputs as inp
+    rows = {}
+    fbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for idx, (name, w) in enumerate(inp.WORKLOADS.items()):
+        (_, _, _, bits), t = device_inputs(torch, dev, w, w.seed(idx))
+        qd, kd, vd, md, o, lse = t
+
+        def step():
+            af.attn_fwd(qd, kd, vd, o, lse, md, causal=w.causal, scale=w.scale)
+
+        ms = launch_times(torch, dev, step, warmup, timed, fbuf if needs_flush(w) else None)
+        af.attn_check()
+        live = live_fraction(w, bits)
+        med = statistics.median(ms)
+        rf = roofline(w, med / 1e3, live)
+        row = {"ms_median": med, "ms_mean": statistics.mean(ms), "value": w.flops() / (med / 1e3) / 1e12,
+               "unit": "TFLOPS", "bound": rf["bound"], "achieved": rf["achieved"], "achieved_unit": rf["unit"],
+               "frac": rf["frac"], "frac_of_mean": rf["frac"] * med / statistics.mean(ms),
+               "live_fraction": live, "launches": timed * kernels_per_step(w)}
+        if w.mask != "none":
+            row["tiles"] = skip_counts(af, torch, dev, w, t)
+        rows[name] = row
+        del t, qd, kd, vd, md, o, lse
+        torch.cuda.empty_cache()
+    return rows
 
 
 def run_ours(args):
@@ -324,13 +447,11 @@ def run_ours(args):
     af.library()  # fail loudly here if the CUDA library is missing
     w, idx = workload(args.workload, args.batch)
     seed = replica_seed(w.seed(idx), rank)
-    q, k, v, bits = w.make(seed)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    md = None if bits is None else torch.from_numpy(bits.view(np.int32)).to(dev)
-    o = torch.empty_like(qd)
-    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
-    flush = algorithmic_bytes(w) <= 2 * L2_BYTES
+    (q, k, v, bits), t = device_inputs(torch, dev, w, seed)
+    qd, kd, vd, md, o, lse = t
+    flush = needs_flush(w)
     fbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+    live = live_fraction(w, bits)
 
     def step():
         af.attn_fwd(qd, kd, vd, o, lse, md, causal=w.causal, scale=w.scale)
@@ -342,22 +463,12 @@ def run_ours(args):
     sampler = ClockSampler(local, enabled=not args.no_clocks)
     time.sleep(0.4 if sampler.proc else 0)
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     barrier(world)
-    torch.cuda.synchronize(dev)
     sampler.mark_start()
-    for i in range(K):
-        if flush:
-            fbuf.fill_(i & 0xFF)
-        starts[i].record()
-        step()
-        ends[i].record()
-    torch.cuda.synchronize(dev)
+    per_launch_ms = launch_times(torch, dev, step, 0, K, fbuf)
     barrier(world)
     sampler.mark_end()
     af.attn_check()
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     t_ms = sum(per_launch_ms)
     t_ms = max_over_ranks(t_ms, world, dev)
     clocks = sampler.stop() if sampler.proc else None
@@ -367,25 +478,35 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, max(3, min(K, 20)), world)
 
+    mean_ms, med_ms = statistics.mean(per_launch_ms), statistics.median(per_launch_ms)
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": t_ms / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": {0: "f16", 1: "bf16"}[w.dtype], "data": "synthetic",
             "config": config_dict(w, args.workload, world),
-            "roofline": roofline(w, statistics.mean(per_launch_ms) / 1e3),
+            "roofline": roofline(w, mean_ms / 1e3, live),
             "gpu_launches": K * kernels_per_step(w), "clocks": clocks, "e2e": e2e, "kernel": kernel_hash()}
-    line["roofline"]["launch_ms_median"] = statistics.median(per_launch_ms)
+    line["roofline"]["launch_ms_mean"] = mean_ms
+    line["roofline"]["launch_ms_median"] = med_ms
+    line["roofline"]["frac_of_median"] = line["roofline"]["frac"] * mean_ms / med_ms
     if kernels_per_step(w) > 1:
         # the events bracket the whole call (mask pre-pass, compaction, attention), so the
         # achieved rate is that of the step, a lower bound for the attention kernel's own
         line["roofline"]["timed"] = "whole step (mask pre-pass + compaction + attention kernel)"
+    if w.mask != "none":
+        line["tiles"] = skip_counts(af, torch, dev, w, t)
+    del t, qd, kd, vd, md, o, lse, fbuf
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, cores, sample, secs = cpu_baseline(w, seed, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample,
-                                "seconds": secs}
+        line["cpu_baseline"] = cpu_baseline(w, seed, args.cpu_seconds)
         if w.B * w.Hq * w.S <= 4096:  # the tiny workload: also the whole oracle on one thread
             line["cpu_baseline"]["single_thread_value"] = cpu_single_thread(w, seed)
     else:
         line["cpu_baseline"] = None
+    if world == 1 and not args.no_sweep:
+        line["sweep"] = run_sweep(af, torch, dev)
+        line["sweep_protocol"] = ("each workload: its seeded inputs, 10 warm-up launches, 50 timed launches (CUDA "
+                                  "events per launch, L2 flushed between launches when a launch's data fits in "
+                                  "twice the L2); value and frac from the median launch")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -32,27 +32,40 @@
  *   - d in {64, 128}; Hq % Hkv == 0; B, Hq, Hkv, S >= 1; scale > 0 and finite.
  *   - dtype: ATTN_F16 or ATTN_BF16 (q, k, v and o share it); accumulation is fp32.
  *   - stream: a cudaStream_t (NULL = the legacy default stream).
- *   - Ownership: the caller owns every buffer; the library keeps no pointer
- *     after the call returns.  Without a custom mask nothing is allocated.  With
- *     one, a pre-pass kernel writes the kept-bit words (mask AND causal AND the
- *     key bound, padded to whole 128-column tiles) and an emptiness map per
- *     (16-row block, 128-column tile), and a compaction kernel lists, per mask row
- *     block, the 16-row blocks that keep anything: the attention kernel computes
- *     only those, packed eight to a 128-row tile, and writes O = 0, LSE = -inf for
- *     the rows of the others without computing them.  All of it lives in
- *     stream-ordered scratch -- cudaMallocAsync / cudaFreeAsync on `stream` -- of
- *     the "custom-mask scratch size": with nm mask row blocks (B, or B*Hq for
- *     per-head masks), R = ceil(Sq/16), T = ceil(Sq/128), U = ceil(Sq/256) and
- *     N = ceil(Sk/128), the sum of nm*Sq*N*16, nm*R*N, nm*R, nm*U*64 and nm*T*N
- *     bytes, each rounded up to a multiple of 256 (Sq = Sk = S for attn_fwd).
- *     It is released in stream order after the attention kernel.
+ *   - Ownership: the caller owns every buffer; the library keeps no pointer to
+ *     them after the call returns.  The library's own state is small and cached:
+ *     tensor maps (TMA descriptors) keyed by buffer address, shape and tile box,
+ *     reused by later calls on the same buffers (a map holds only these, so a
+ *     cached one stays valid); a status word per (device, stream); and, per
+ *     (device, stream) that has run a custom mask, one workspace.  Without a
+ *     custom mask nothing is allocated.  With one, a pre-pass kernel writes the
+ *     kept-bit words (mask AND causal AND the key bound, padded to whole
+ *     128-column tiles) and an emptiness map per (16-row block, 128-column tile),
+ *     and a compaction kernel lists, per mask row block, the 16-row blocks that
+ *     keep anything: the attention kernel computes only those, packed eight to a
+ *     128-row tile, and writes O = 0, LSE = -inf for the rows of the others
+ *     without computing them.  That output lives in the stream's workspace, of at
+ *     least the "custom-mask scratch size": with nm mask row blocks (B, or B*Hq
+ *     for per-head masks), R = ceil(Sq/16), T = ceil(Sq/128), U = ceil(Sq/256)
+ *     and N = ceil(Sk/128), the sum of nm*Sq*N*16, nm*R*N, nm*R, nm*U*64 and
+ *     nm*T*N bytes, each rounded up to a multiple of 256 (Sq = Sk = S for
+ *     attn_fwd).  The workspace is a stream-ordered allocation (cudaMallocAsync
+ *     on `stream`, whole MiB) made by the first custom-mask call on the stream
+ *     and reused by every later one; a call that needs more frees the old block
+ *     in stream order (cudaFreeAsync) and allocates a larger one.  Repeated calls
+ *     of one shape therefore allocate nothing after the first.  The workspace is
+ *     held until attn_release_workspace(stream) or process exit: release it
+ *     before destroying a stream that has run custom masks.
  *   - Errors: arguments are validated before any launch (ATTN_ERR_INVALID /
  *     ATTN_ERR_UNSUPPORTED, nothing launched); a failed launch returns
  *     ATTN_ERR_CUDA.  The work is asynchronous: a kernel that gives up on a
- *     barrier wait (see attn_set_wait_timeout_ns) records ATTN_ERR_TIMEOUT in a
- *     device status word that attn_check() reports.  The library never traps
- *     and never exits the process.
- *   - Thread safety: calls on different streams may run concurrently.
+ *     barrier wait (see attn_set_wait_timeout_ns) records ATTN_ERR_TIMEOUT in
+ *     the status word of the stream it was launched on, which attn_check(that
+ *     stream) reports.  The library never traps and never exits the process.
+ *   - Thread safety: calls on different streams may run concurrently, and so may
+ *     host threads calling on one stream (the library's caches are guarded by
+ *     mutexes), except attn_fwd_noalloc with a custom mask: its calls share one
+ *     fixed array and must not overlap on the GPU (see below).
  */
 #ifndef ATTN_H
 #define ATTN_H
@@ -163,12 +176,17 @@ int attn_fwd_visited(const void *q, const void *k, const void *v, void *o, float
  * every GPU that loads it, held until the process exits, instead of into
  * stream-ordered scratch; calls whose custom-mask scratch size (see the
  * conventions above) exceeds it return ATTN_ERR_INVALID before any launch.
- * The first call on a device looks the array's device address up (once, with
- * that device current); make that first call before any stream capture.  Every
- * call shares the one array and it keeps the last call's contents (each call
- * rewrites every byte it then reads, so nothing needs clearing); calls whose
- * work overlaps on the GPU -- on different streams, say -- race on it, so order
- * them.  The pages this library follows have no counterpart of this entry point.
+ * Every call looks the array's device address up with the caller's device
+ * current (a cheap host call, so a reset or replaced context never sees a stale
+ * address); the first call on a device also loads the library's device code
+ * there, so make it before any stream capture.  Every call shares the one array
+ * and it keeps the last call's contents (each call rewrites every byte it then
+ * reads, so nothing needs clearing); calls whose work overlaps on the GPU -- on
+ * different streams, say -- race on it, so order them.  It makes no host-side
+ * allocation either: on a stream that attn_fwd has not used, its timeout status
+ * goes to the status word shared by such streams, which attn_check reports for
+ * any of them.  The pages this library follows have no counterpart of this
+ * entry point.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
 int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -176,11 +194,31 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
                      float scale, int dtype, void *stream);
 
 /*
- * attn_check -- synchronise `stream`, then report (and clear) the device status
- * word of the current device: ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if
- * the stream itself reports an error.
+ * attn_check -- read (and clear) the status word of `stream` on the current
+ * device, in stream order after the work enqueued on it so far, and synchronise
+ * the stream: ATTN_OK, ATTN_ERR_TIMEOUT if a launch on this stream gave up on a
+ * barrier wait, or ATTN_ERR_CUDA if the stream itself reports an error.  Launches
+ * on other streams do not affect it (streams share a word only past the first
+ * 1023 distinct streams of a device, and for attn_fwd_noalloc calls on streams
+ * attn_fwd has not used).
  */
 int attn_check(void *stream);
+
+/*
+ * attn_release_workspace -- free (in stream order, cudaFreeAsync on `stream`) the
+ * custom-mask workspace the library holds for `stream` on the current device, if
+ * any.  Call it before destroying a stream that ran custom masks; a later call on
+ * the stream simply allocates a new one.  ATTN_OK, or ATTN_ERR_CUDA.
+ */
+int attn_release_workspace(void *stream);
+
+/*
+ * attn_debug_counters -- host-side counters since the library was loaded, for
+ * tests and tuning: out[0] = workspace allocations, out[1] = tensor maps encoded,
+ * out[2] = tensor maps served from the cache; entries past 2 are set to 0.
+ * n = the number of entries of `out` (>= 1).
+ */
+int attn_debug_counters(unsigned long long *out, int n);
 
 /* attn_strerror -- a static, human-readable string for a status code. */
 const char *attn_strerror(int status);

@@ -40,6 +40,21 @@ def oracle_rows(q, k, v, bits, causal, scale, dtype, rows):
                             float(np.float32(scale)))
 
 
+def stratified_rows(B, Hq, S, seed):
+    """Flat row ids (b*Hq + hq)*S + i for every (b, hq): one seeded random row from every
+    32-row warp slice (so every warp of both Q tiles of every 256-row work unit, and every
+    unit of every CTA's walk, is represented), plus rows 0, 1, 127, 128 (the Q-tile seam),
+    255, 256 (the unit seam), S-256 and S-1."""
+    rng = np.random.default_rng(int(seed) + 11)
+    nsl = -(-S // 32)
+    fixed = np.array(sorted({r for r in (0, 1, 127, 128, 255, 256, S - 256, S - 1) if 0 <= r < S}), np.int64)
+    out = []
+    for bh in range(B * Hq):
+        pick = np.minimum(32 * np.arange(nsl) + rng.integers(0, 32, size=nsl), S - 1)
+        out.append(bh * S + np.unique(np.concatenate([pick, fixed])))
+    return np.concatenate(out)
+
+
 def assert_close(o, lse, o_ref, lse_ref, what=""):
     """The parity bar: |O - O_ref| <= 1e-2 + 1e-2*|O_ref| elementwise, |LSE - LSE_ref| <= 1e-3,
     -inf LSE exactly where the oracle has it, and no NaN/Inf anywhere else."""

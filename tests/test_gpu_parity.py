@@ -1,8 +1,10 @@
 """CUDA path vs the fp64 oracle, element by element, through the C-ABI.
 
-Small cases are checked on every output; the full-size workloads of the pages'
-benchmarks are checked on seeded row samples (every (batch, head) pair: rows
-0, 1, 127, 128, S-1 plus random rows), launched exactly as bench.py launches them.
+Small cases are checked on every output.  The full-size workloads of the pages'
+benchmarks are launched exactly as bench.py launches them and checked on a stratified
+row sample (every (batch, head) pair: one row from every 32-row warp slice, plus the
+tile and unit seams and the last rows); one of them (causal MHA, S = 4096) is checked on
+every row.
 """
 import numpy as np
 import pytest
@@ -10,7 +12,7 @@ import torch
 
 from attention_forward_07_gb300 import inputs as inp
 
-from gpu_util import assert_close, expected_visited, oracle_full, oracle_rows, run_cuda
+from gpu_util import assert_close, expected_visited, oracle_full, oracle_rows, run_cuda, stratified_rows
 
 import oracle
 
@@ -139,9 +141,23 @@ def test_prefill_workloads_sampled_parity(name):
     w = inp.WORKLOADS[name]
     q, k, v, bits = w.make(w.seed(list(inp.WORKLOADS).index(name)))
     o, lse = run_cuda(q, k, v, bits, w.causal, w.scale)
-    rows = inp.sample_rows(w.B, w.Hq, w.S, 4, seed=w.S)
+    rows = stratified_rows(w.B, w.Hq, w.S, seed=w.S)
     o_ref, lse_ref = oracle_rows(q, k, v, bits, w.causal, w.scale, w.dtype, rows)
     assert_close(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, name)
     # properties that hold at any size, checked on every row: finite outputs, |O| <= max|V|
     vmax = float(v.float().abs().max())
     assert np.all(np.isfinite(lse)) and np.abs(o).max() <= vmax * (1 + 1e-2)
+
+
+def test_prefill_every_row_mha_causal_S4096():
+    """Causal MHA, B=8, H=16, S=4096 (one of the pages' prefill configurations) compared
+    with the oracle on all 524288 rows, one batch entry at a time."""
+    name = "mha_causal_S4096"
+    w = inp.WORKLOADS[name]
+    q, k, v, bits = w.make(w.seed(list(inp.WORKLOADS).index(name)))
+    o, lse = run_cuda(q, k, v, bits, w.causal, w.scale)
+    per_b = w.Hq * w.S
+    for b in range(w.B):
+        rows = np.arange(b * per_b, (b + 1) * per_b, dtype=np.int64)
+        o_ref, lse_ref = oracle_rows(q, k, v, bits, w.causal, w.scale, w.dtype, rows)
+        assert_close(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, f"{name} b={b}")

@@ -71,3 +71,33 @@ def test_bench_helpers_without_a_gpu():
     assert bench.config_key(w) == "B4_Hq32_Hkv8_S8192_d128_causal_none"
     r = bench.roofline(inp.WORKLOADS["short_masked"], 60e-6)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+
+
+def test_bench_algorithmic_units_of_the_masked_workloads():
+    """The 90 %-masked workload's algorithmic bytes count the Q rows of the 16-row blocks that
+    keep anything (measured from the mask), not the whole Q; the live fraction is exact on a
+    hand-built mask."""
+    import importlib.util
+    import os
+    import numpy as np
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from dataclasses import replace
+    from attention_forward_07_gb300 import inputs as inp
+    w = replace(inp.WORKLOADS["short_masked90"], B=2, S=40)
+    keep = np.ones((2, 40, 40), bool)
+    keep[0, 0:16] = False          # block 0 of entry 0 keeps nothing
+    keep[1, 32:40] = False         # the ragged last block of entry 1 keeps nothing
+    keep[1, 20, :] = False         # one empty row inside a live block does not empty it
+    assert bench.live_fraction(w, inp.pack_bits(keep)) == 4 / 6
+    assert bench.live_fraction(w, None) == 1.0
+    w90 = inp.WORKLOADS["short_masked90"]
+    _, _, _, bits = w90.make(w90.seed(list(inp.WORKLOADS).index("short_masked90")))
+    live = bench.live_fraction(w90, bits)
+    assert 0.15 < live < 0.25
+    q_bytes = w90.B * w90.Hq * w90.S * w90.d * 2
+    assert bench.algorithmic_bytes(w90) - bench.algorithmic_bytes(w90, live) == q_bytes - round(q_bytes * live)
+    r = bench.roofline(w90, 49.3e-6, live)
+    assert r["bound"] == "hbm" and r["algorithmic_bytes"] == bench.algorithmic_bytes(w90, live)
