@@ -60,13 +60,11 @@ constexpr int QT = 2;          // Q tiles per work unit
 constexpr int UNIT_ROWS = BM * QT;
 constexpr int BN = 128;        // keys per K/V tile
 constexpr int NTHREADS = 384;  // 12 warps
-constexpr int REGS_LAUNCH = 168, REGS_LOADMMA = 88, REGS_SOFTMAX = 208;
-static_assert(128 * REGS_LOADMMA + 256 * REGS_SOFTMAX <= NTHREADS * REGS_LAUNCH, "register split");
+constexpr int REGS_LAUNCH = 168;
 constexpr int NINFO = 4;       // depth of the tile-descriptor ring
 constexpr int TMEM_COLS = 512;
-constexpr int S_COL0 = 0;      // S_t (fp32, 128 columns) at t*128; P_t aliases its first 64
-constexpr int O_COL0 = 256;    // O_t (fp32, d columns) at 256 + t*128
 constexpr int FLAG_END = 4;    // info entry marking the end of a work unit
+constexpr int FLAG_EXIT = 8;   // info entry telling the consumers that no unit is left
 constexpr float LN2 = 0.69314718055994530942f;
 
 // NONE: every key; CAUSAL: keys up to the aligned position; BAND: keys in
@@ -88,6 +86,22 @@ struct Layout {
   // fp16/bf16 = exactly one buffer); the buffer is released when those warps are done.
   static constexpr bool STAGE_O = (QBUF == 2);
   static constexpr int QEMPTY_COUNT = 1 + (STAGE_O ? QT * 4 : 0);  // MMA commit + softmax warps
+  // TMEM.  d = 128: S_t (fp32, 128 columns) at t * 128, P_t (fp16/bf16 pairs) over its first 64
+  // columns, O_t at 256 + t * 128.  d = 64: a ring of three S slots at 0, 128, 256 shared by the
+  // two Q tiles (the n-th Q.K^T of the CTA goes to slot n % 3, its P over the slot's first 64
+  // columns), O_t at 384 + t * 64: a Q tile's next Q.K^T runs while its softmax works on the
+  // current one.
+  static constexpr bool RING = (D == 64);
+  static constexpr int S_SLOTS = RING ? 3 : QT;
+  static constexpr int O_COL = RING ? 384 : 256;
+  static constexpr int O_STRIDE = RING ? 64 : 128;
+  static_assert(S_SLOTS * 128 + QT * O_STRIDE <= TMEM_COLS, "TMEM columns");
+  // Registers per thread after setmaxnreg: the load / MMA warpgroup and the two softmax
+  // warpgroups share the launch's 384 x 168 (the ring bookkeeping of d = 64 costs the MMA
+  // warp a few; its softmax, with a 64-column O, needs fewer).
+  static constexpr int REGS_LOADMMA = (D == 64) ? 96 : 88;
+  static constexpr int REGS_SOFTMAX = (D == 64) ? 200 : 208;
+  static_assert(128 * REGS_LOADMMA + 256 * REGS_SOFTMAX <= NTHREADS * REGS_LAUNCH, "register split");
   // With one Q buffer (d = 128) the epilogue stages O through a 32 KiB area of its own,
   // 4 KiB per softmax warp, one 64-column half at a time (custom masks need that room for
   // their mask words and write O directly).
@@ -111,8 +125,9 @@ struct Layout {
                        B_KEMPTY = B_KFULL + KSLOT, B_VFULL = B_KEMPTY + KSLOT,
                        B_VEMPTY = B_VFULL + VSLOT, B_IFULL = B_VEMPTY + VSLOT,
                        B_IEMPTY = B_IFULL + NINFO,
-                       B_STILE = B_IEMPTY + NINFO, B_PREADY = B_STILE + QT,
-                       B_ODONE = B_PREADY + QT, B_DRAIN = B_ODONE + QT, NBAR = B_DRAIN + 1;
+                       B_STILE = B_IEMPTY + NINFO, B_PREADY = B_STILE + S_SLOTS,
+                       B_ODONE = B_PREADY + QT, B_OPV = B_ODONE + QT, B_DRAIN = B_OPV + QT,
+                       NBAR = B_DRAIN + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
@@ -127,7 +142,8 @@ struct InfoHdr {
   int flags;  // bit t: Q tile t computes this key tile; FLAG_END: end of unit
   int sq, sk;  // the unit's query and key lengths (per batch entry with seqlens arrays)
   int qoff;    // packed layouts: the entry's first row in q / o / lse
-  int pad[3];
+  int bh, qb;  // the work unit this entry belongs to: b * Hq + hq, 256-row block
+  int pad;
 };
 static_assert(sizeof(InfoHdr) == 32, "descriptor slot size");
 
@@ -164,6 +180,7 @@ struct Params {
   int causal;      // the band only bounds keys on the right: longest units first
   int inject;
   int status_slot;  // index into g_attn_status of the stream this launch runs on
+  int dynamic;      // 1: units are taken from the slot's work queue (g_sched), else a fixed walk
   float scale_log2;
   uint32_t timeout_us;  // longest barrier wait (microseconds; 32 bits keep it in one register)
 };
@@ -174,6 +191,10 @@ struct Params {
 // slot; streams beyond the table share slot 0): bit 0 = a barrier wait ran out of time.
 constexpr int STATUS_SLOTS = 1024;
 __device__ unsigned int g_attn_status[STATUS_SLOTS];
+// Work queue per stream slot: [2 s] = next unit to hand out, [2 s + 1] = CTAs that have
+// finished.  Launches on one stream run one after the other, so a slot serves one launch at
+// a time; its last CTA resets both words for the next launch.
+__device__ unsigned int g_sched[2 * STATUS_SLOTS];
 
 namespace attn {
 
@@ -223,12 +244,37 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
   return u < num_units ? u : -1;
 }
 
-// Unit -> (batch, query head, 256-row block).  Causal: block index descending (the
-// longest units first), heads of a block adjacent.  Otherwise: consecutive units walk
-// the blocks and the heads of one K/V head, so concurrent CTAs share K/V through L2.
+// Unit -> (batch, query head, 256-row block).
+// Not causal: consecutive units walk the blocks and the query heads of one K/V head, so the
+// CTAs running at one time share K/V through L2.
+// Causal with the fixed walk: block index descending (the longest units first), the heads of
+// a block adjacent.
+// Causal with the work queue: bands of blocks from the longest down, each band half of the
+// blocks left (at least one): [nqb - w0, nqb), then w1 = ceil(rest / 2) below it, and so on,
+// so the last units handed out are the shortest.  Inside a band the units go K/V head by K/V
+// head (b, hkv), and for one K/V head the band's blocks longest first with the g query heads
+// of a block adjacent: the CTAs running at one time read a few K/V heads, which stay in L2,
+// and CTAs that finish early take the next unit, which keeps the load balanced.
 __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, int& b, int& hq,
                                             int& qb) {
-  if (causal) {
+  if (causal && p.dynamic) {
+    const int G = p.B * p.Hkv;
+    int hi = p.nqb, base = 0;
+    while (true) {
+      const int w = (hi + 1) / 2;
+      const int n = G * p.g * w;
+      if (u < base + n || hi - w <= 0) {
+        const int v = u - base, per_group = p.g * w;
+        const int grp = v / per_group, r = v % per_group;
+        qb = hi - 1 - r / p.g;
+        b = grp / p.Hkv;
+        hq = (grp % p.Hkv) * p.g + r % p.g;
+        return;
+      }
+      base += n;
+      hi -= w;
+    }
+  } else if (causal) {
     const int bh = u % (p.B * p.Hq);
     qb = p.nqb - 1 - u / (p.B * p.Hq);
     b = bh / p.Hq;
@@ -242,6 +288,15 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
     b = bk / p.Hkv;
     hq = hkv * p.g + member;
   }
+}
+
+// The load warp's next unit (the same value in every lane), or -1 when none is left.
+__device__ __forceinline__ int next_unit(const Params& p, int k, int lane) {
+  if (!p.dynamic) return unit_at(k, p.num_units);
+  unsigned int x = 0;
+  if (lane == 0) x = atomicAdd(&g_sched[2 * p.status_slot], 1u);
+  x = __shfl_sync(0xffffffffu, x, 0);
+  return x < (unsigned int)p.num_units ? (int)x : -1;
 }
 
 // Query / key lengths of batch entry b and, for packed layouts, its first query and key row
@@ -314,8 +369,19 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
   bool inject = p.inject != 0;
 
   for (int k = 0;; ++k) {
-    const int u = unit_at(k, p.num_units);
-    if (u < 0) break;
+    const int u = next_unit(p, k, lane);
+    if (u < 0) {
+      // no unit left: an exit descriptor releases the MMA warp and the softmax warpgroups
+      if (!bwait_warp(bars + 8u * (L::B_IEMPTY + ie), ie_par, abort_flag, to)) goto drain;
+      if (lane == 0) {
+        hdr[ie].j = -1;
+        hdr[ie].flags = FLAG_EXIT;
+        mbar_arrive(bars + 8u * (L::B_IFULL + ie));
+      }
+      __syncwarp();
+      if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
+      break;
+    }
     int b, hq, qb;
     decode_unit(u, p, causal, b, hq, qb);
     const int hkv = hq / p.g;
@@ -424,6 +490,8 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
         hdr[ie].sq = sq;
         hdr[ie].sk = sk;
         hdr[ie].qoff = qoff;
+        hdr[ie].bh = b * p.Hq + hq;
+        hdr[ie].qb = qb;
         const uint32_t fb = bars + 8u * (L::B_IFULL + ie);
         if constexpr (MODE == MASK_CUSTOM) {
           mbar_expect_tx(fb, L::WORDS_PER_ENTRY * 4);
@@ -485,6 +553,8 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       hdr[ie].sq = sq;
       hdr[ie].sk = sk;
       hdr[ie].qoff = qoff;
+      hdr[ie].bh = b * p.Hq + hq;
+      hdr[ie].qb = qb;
       mbar_arrive(bars + 8u * (L::B_IFULL + ie));
     }
     __syncwarp();
@@ -514,16 +584,21 @@ namespace attn {
 // ------------------------------------------------------------------ MMA issuer (warp 1)
 // The whole warp runs this code converged (descriptors in uniform registers); elect.sync
 // picks the lane that issues each tcgen05 instruction.  Per tile descriptor e (key tile j)
-// and Q tile t, in this order:
-//   O_t (+)= P_t(prev) . V(prev)    once softmax t has written P for the previous tile
-//   S_t     = Q_t . K(j)^T          then signal softmax t
-// so S_t / P_t (which share TMEM columns) are rewritten only after the P.V that reads
-// them.  Each ring slot is released by a commit right after its last reader.
+// and Q tile t:
+//   d = 128:  O_t (+)= P_t(prev) . V(prev)   once softmax t has written P for the previous tile,
+//             S_t     = Q_t . K(j)^T         then signal softmax t;
+//             S_t / P_t share TMEM columns, so S_t is rewritten only after the P.V that reads it.
+//   d = 64:   S(n)    = Q_t . K(j)^T         into ring slot n % 3 (the CTA's n-th Q.K^T),
+//             O_t (+)= P_t(prev) . V(prev)   from the slot of the previous tile's S,
+//             so the next S of a Q tile is computed while its softmax still works on the
+//             current one.  At most two slots hold an S or P whose P.V is not yet issued when
+//             a Q.K^T is issued, so the third is free; each P.V is followed by a commit on
+//             OPV(t), which the softmax waits for before it rescales O_t.
+// Each ring slot of K / V is released by a commit right after its last reader.
 template <int D, bool BF16, int MODE>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t* gbase,
                                          volatile int* abort_flag, uint32_t tmem, int lane) {
   using L = Layout<D, MODE>;
-  const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
   const uint32_t to = p.timeout_us;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -532,12 +607,18 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
 
   uint32_t q_par = 0, ie_par = 0, kpar = 0, vpar = 0, p_par0 = 0, p_par1 = 0;  // q_par: bit per Q buffer
   int kslot = 0, vslot = 0, ie = 0;
+  int nqk = 0;                 // d = 64: ring slot of the next Q.K^T
+  int pslot0 = 0, pslot1 = 0;  // d = 64: ring slot holding P_t of the previous key tile
 
   for (int k = 0;; ++k) {
-    const int u = unit_at(k, p.num_units);
-    if (u < 0) break;
-    int b, hq, qb;
-    decode_unit(u, p, causal, b, hq, qb);
+    // the unit's first descriptor names it (the loop below waits on it again, at once)
+    if (!bwait_warp(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) goto drain;
+    if (hdr[ie].flags & FLAG_EXIT) {
+      mbar_arrive_elect(bars + 8u * (L::B_IEMPTY + ie));
+      break;
+    }
+    const int bh = hdr[ie].bh, qb = hdr[ie].qb;
+    const int b = bh / p.Hq, hq = bh - b * p.Hq;
     const int qbuf = k % L::QBUF;
     if (!bwait_warp(bars + 8u * (L::B_QFULL + qbuf), (q_par >> qbuf) & 1u, abort_flag, to)) goto drain;
     q_par ^= 1u << qbuf;
@@ -568,47 +649,65 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
 
 #pragma unroll
       for (int t = 0; t < QT; ++t) {
-        const uint32_t s_col = tmem + S_COL0 + t * 128;
-        if (have_prev && ((prev_flags >> t) & 1)) {
-          uint32_t& pp = t ? p_par1 : p_par0;
-          if (!bwait_warp(bars + 8u * (L::B_PREADY + t), pp, abort_flag, to)) goto drain;
-          pp ^= 1u;
-          tc_fence_after();
-          bool& started = t ? pv1 : pv0;
-          const uint32_t vbase = base + L::OFF_V + prev_vslot * L::KV_TILE_BYTES;
-          // V tile as the MN-major B operand: 16 keys per step (2048 bytes), the two
-          // 64-column halves of d are KV_TILE_BYTES/2 apart, 8-key groups 1024 apart.
+        int& pslot = t ? pslot1 : pslot0;
+        int new_slot = t;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts_elect(tmem + O_COL0 + t * 128, s_col + kk * 8,
-                         sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
-                         (started || kk > 0) ? 1u : 0u);
-          started = true;
+        for (int step = 0; step < 2; ++step) {
+          // d = 64 issues this tile's Q.K^T first, d = 128 its P.V first
+          if ((step == 0) == L::RING) {
+            if (!end && ((flags >> t) & 1)) {
+              if (!k_ready) {
+                if (!bwait_warp(bars + 8u * (L::B_KFULL + cur_kslot), cur_kpar, abort_flag, to)) goto drain;
+                tc_fence_after();
+                k_ready = true;
+              }
+              if constexpr (L::RING) {
+                new_slot = nqk;
+                nqk = nqk == L::S_SLOTS - 1 ? 0 : nqk + 1;
+              }
+              const uint32_t s_col = tmem + new_slot * 128;
+              const uint32_t qbase = base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES;
+              const uint32_t kbase = base + L::OFF_K + cur_kslot * L::KV_TILE_BYTES;
+              // Q and K as K-major operands: 16 elements (32 bytes) per step inside a
+              // 128-byte swizzle row, the next 64 elements one half-tile further.
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+                mma_ss_elect(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                             ID_QK, kk > 0 ? 1u : 0u);
+              }
+              tc_commit_elect(bars + 8u * (L::B_STILE + new_slot));
+              if (p.visited && lane == 0)
+                p.visited[((size_t)(b * p.Hq + hq) * p.nqt + (qb * QT + t)) * p.nkt + j] = 1;
+              __syncwarp();
+            }
+          } else {
+            if (have_prev && ((prev_flags >> t) & 1)) {
+              uint32_t& pp = t ? p_par1 : p_par0;
+              if (!bwait_warp(bars + 8u * (L::B_PREADY + t), pp, abort_flag, to)) goto drain;
+              pp ^= 1u;
+              tc_fence_after();
+              bool& started = t ? pv1 : pv0;
+              const uint32_t p_col = tmem + (L::RING ? pslot : t) * 128;
+              const uint32_t vbase = base + L::OFF_V + prev_vslot * L::KV_TILE_BYTES;
+              // V tile as the MN-major B operand: 16 keys per step (2048 bytes), the two
+              // 64-column halves of d are KV_TILE_BYTES/2 apart, 8-key groups 1024 apart.
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts_elect(tmem + L::O_COL + t * L::O_STRIDE, p_col + kk * 8,
+                             sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
+                             (started || kk > 0) ? 1u : 0u);
+              started = true;
+              if constexpr (L::RING) tc_commit_elect(bars + 8u * (L::B_OPV + t));
+            }
+            // end of unit: O_t is complete once its last P.V is -- signal it now, so softmax t
+            // starts its epilogue without waiting for the other Q tile's P.V
+            if (end && (t ? pv1 : pv0)) tc_commit_elect(bars + 8u * (L::B_ODONE + t));
+            if (t == QT - 1 && have_prev) tc_commit_elect(bars + 8u * (L::B_VEMPTY + prev_vslot));
+          }
         }
-        // end of unit: O_t is complete once its last P.V is -- signal it now, so softmax t
-        // starts its epilogue without waiting for the other Q tile's P.V
-        if (end && (t ? pv1 : pv0)) tc_commit_elect(bars + 8u * (L::B_ODONE + t));
-        if (t == QT - 1 && have_prev) tc_commit_elect(bars + 8u * (L::B_VEMPTY + prev_vslot));
-        if (!end && ((flags >> t) & 1)) {
-          if (!k_ready) {
-            if (!bwait_warp(bars + 8u * (L::B_KFULL + cur_kslot), cur_kpar, abort_flag, to)) goto drain;
-            tc_fence_after();
-            k_ready = true;
-          }
-          const uint32_t qbase = base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES;
-          const uint32_t kbase = base + L::OFF_K + cur_kslot * L::KV_TILE_BYTES;
-          // Q and K as K-major operands: 16 elements (32 bytes) per step inside a
-          // 128-byte swizzle row, the next 64 elements one half-tile further.
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-            mma_ss_elect(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                         ID_QK, kk > 0 ? 1u : 0u);
-          }
-          tc_commit_elect(bars + 8u * (L::B_STILE + t));
-          if (p.visited && lane == 0)
-            p.visited[((size_t)(b * p.Hq + hq) * p.nqt + (qb * QT + t)) * p.nkt + j] = 1;
-          __syncwarp();
+        if constexpr (L::RING) {
+          if (!end && ((flags >> t) & 1)) pslot = new_slot;
         }
       }
       if (!end) tc_commit_elect(bars + 8u * (L::B_KEMPTY + cur_kslot));
@@ -644,36 +743,48 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
                                              int quarter, int lane) {
   using L = Layout<D, MODE>;
   using OutT = uint16_t;
-  const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
   const uint32_t to = p.timeout_us;
   const uint32_t bars = base + L::OFF_BAR;
   const uint32_t* words = reinterpret_cast<const uint32_t*>(gbase + L::OFF_WORDS);
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
   const int r = quarter * 32 + lane;
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-  const uint32_t s_addr = tmem + lane_off + S_COL0 + t * 128;
-  const uint32_t o_addr = tmem + lane_off + O_COL0 + t * 128;
+  const uint32_t o_addr = tmem + lane_off + L::O_COL + t * L::O_STRIDE;
   const float c = p.scale_log2;
 
   uint32_t s_par = 0, o_par = 0, ie_par = 0;
   int ie = 0;
+  int nq = 0;  // d = 64: Q.K^T the MMA warp has issued before the current descriptor's
+  int np = 0;  // d = 64: P tiles this thread's Q tile has produced (one P.V, one OPV phase each)
 
   for (int k = 0;; ++k) {
-    const int u = unit_at(k, p.num_units);
-    if (u < 0) break;
-    int b, hq, qb;
-    decode_unit(u, p, causal, b, hq, qb);
+    // the unit's first descriptor names it (the loop below waits on it again, at once)
+    if (!bwait_warp(bars + 8u * (L::B_IFULL + ie), ie_par, abort_flag, to)) return;
+    if (hdr[ie].flags & FLAG_EXIT) {
+      mbar_arrive(bars + 8u * (L::B_IEMPTY + ie));
+      break;
+    }
+    const int bh = hdr[ie].bh, qb = hdr[ie].qb;
+    const int b = bh / p.Hq, hq = bh - b * p.Hq;
     const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
     // This thread's query row.  Custom masks: the tile holds compacted slots, 16 rows each;
     // blk_a / blk_b are the original blocks of this warp's two slots (-1: no such slot).
     int i = qb * UNIT_ROWS + t * BM + r;
     int blk_a = 0, blk_b = 0;
+    bool live_a = true, live_b = true;  // this warp's own two 16-row blocks keep something
+    const int hb0 = (qb * UNIT_ROWS + t * BM + quarter * 32) / 16;
     if constexpr (MODE == MASK_CUSTOM) {
       const int* rm = p.rowmap + ((size_t)mb * p.nqb + qb) * 16 + t * 8 + quarter * 2;
       blk_a = __ldg(rm);
       blk_b = __ldg(rm + 1);
       const int blk = lane < 16 ? blk_a : blk_b;
       i = blk >= 0 ? blk * 16 + (lane & 15) : -1;
+      if constexpr (D == 64) {
+        // read now, used by the epilogue (the loads overlap the unit's first tile; d = 128
+        // has no registers to spare and reads them at the epilogue)
+        live_a = hb0 >= p.nr16 || __ldg(p.live + (size_t)mb * p.nr16 + hb0) != 0;
+        live_b = hb0 + 1 >= p.nr16 || __ldg(p.live + (size_t)mb * p.nr16 + hb0 + 1) != 0;
+      }
     }
     float m = -INFINITY, l = 0.f;
     int nact = 0;
@@ -695,10 +806,21 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       mbar_arrive(bars + 8u * (L::B_IEMPTY + ie));
       if (++ie == NINFO) { ie = 0; ie_par ^= 1u; }
       if (end) break;
+      // where this tile's S is: its own columns (d = 128), or the ring slot of its Q.K^T
+      // (d = 64: the MMA warp issues Q_0 K^T before Q_1 K^T for each descriptor)
+      int slot = t;
+      uint32_t spar = s_par;
+      if constexpr (L::RING) {
+        const int before = nq + ((t == 1 && (flags & 1)) ? 1 : 0);
+        slot = before % L::S_SLOTS;
+        spar = (uint32_t)(before / L::S_SLOTS) & 1u;
+        nq += (flags & 1) + ((flags >> 1) & 1);
+      }
       if (!act) continue;
+      const uint32_t s_addr = tmem + lane_off + slot * 128;
 
-      if (!bwait_warp(bars + 8u * (L::B_STILE + t), s_par, abort_flag, to)) return;
-      s_par ^= 1u;
+      if (!bwait_warp(bars + 8u * (L::B_STILE + slot), spar, abort_flag, to)) return;
+      if constexpr (!L::RING) s_par ^= 1u;
       tc_fence_after();
       // Scores: the first 64 columns are loaded and reduced while the last 64 are in flight.
       uint32_t sr[128];
@@ -757,6 +879,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
 
       // Correction: rescale this row of O (only warps where some row moved its base).
       if (nact > 0 && __any_sync(0xffffffffu, grow)) {
+        if constexpr (L::RING) {
+          // d = 64: this tile's S was computed before the previous P.V was issued; wait
+          // until that P.V (OPV phase np - 1, the latest that can have completed) is done
+          if (!bwait_warp(bars + 8u * (L::B_OPV + t), (uint32_t)(np - 1) & 1u, abort_flag, to)) return;
+          tc_fence_after();
+        }
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int ch = 0; ch < D / 16; ++ch) {
@@ -804,8 +932,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       l = l * alpha + sum;
       m = m_new;
       tc_fence_before();
+      // d = 64: the next S may already be there, so a fast warp could start the next tile
+      // and arrive again before the slowest warp has arrived for this one; the warpgroup
+      // meets here first
+      if constexpr (L::RING) named_bar_sync(1 + t, BM);
       mbar_arrive(bars + 8u * (L::B_PREADY + t));
       ++nact;
+      ++np;
     }
 
     // Epilogue: O = O_acc / l, LSE; rows with nothing kept give O = 0, LSE = -inf.
@@ -816,7 +949,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     }
     const bool row_ok = i >= 0 && i < sq;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    if (L::STAGE_O && nact > 0) {
+    bool staged = false;
+    if constexpr (L::STAGE_O) {
+     if (nact > 0) {
+      staged = true;
       // This warp's 32 rows x d go through its slice of the unit's Q buffer (the unit's
       // last Q.K^T of tile t finished before O_t was signalled; a tile that computed
       // nothing never waited for its Q load, so it writes its zeros directly instead):
@@ -827,14 +963,15 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       constexpr int ROW_BYTES = D * 2, CHUNKS = ROW_BYTES / 16;
       static_assert(QT * 4 * 32 * ROW_BYTES == L::Q_BUF_BYTES, "staging slices fill one Q buffer");
       uint8_t* stage = gbase + L::OFF_Q + (k % L::QBUF) * L::Q_BUF_BYTES + (t * 4 + quarter) * (32 * ROW_BYTES);
+      static_assert(D == 64, "the staged epilogue reads the whole O row at once");
+      uint32_t ob[64];
+      tmem_ld32x32b_x64_wait(o_addr, ob);  // the whole row of O in one load
 #pragma unroll
       for (int ch = 0; ch < D / 16; ++ch) {
-        uint32_t ob[16];
-        tmem_ld32x32b_x16_wait(o_addr + ch * 16, ob);
         uint32_t pk[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x)
-          pk[x] = pack2<BF16>(__uint_as_float(ob[2 * x]) * inv, __uint_as_float(ob[2 * x + 1]) * inv);
+          pk[x] = pack2<BF16>(__uint_as_float(ob[16 * ch + 2 * x]) * inv, __uint_as_float(ob[16 * ch + 2 * x + 1]) * inv);
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
           const int c = 2 * ch + hc;
@@ -860,6 +997,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       fence_proxy_async_smem();  // the next TMA load into this buffer comes after these accesses
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8u * (L::B_QEMPTY + (k % L::QBUF)));  // slice read back
+     }
+    }
+    if (staged) {
     } else if (L::STAGE_SEP) {
       // Same scheme through the warp's own 4 KiB slice, one 64-column half of d per pass:
       // each store instruction then writes four whole 128-byte segments of O.
@@ -927,11 +1067,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       // were left out of the compacted list: O = 0 and LSE = -inf there, this warp's two
       // blocks written in whole 16-byte chunks by consecutive lanes.
       constexpr int ROW_BYTES = D * 2, CHUNKS = ROW_BYTES / 16;
-      const int hb0 = (qb * UNIT_ROWS + t * BM + quarter * 32) / 16;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int hb = hb0 + hh;
-        if (hb >= p.nr16 || __ldg(p.live + (size_t)mb * p.nr16 + hb)) continue;  // warp-uniform
+        if constexpr (D == 64) {
+          if (hh ? live_b : live_a) continue;  // warp-uniform
+        } else {
+          if (hb >= p.nr16 || __ldg(p.live + (size_t)mb * p.nr16 + hb)) continue;  // warp-uniform
+        }
         uint8_t* ob = reinterpret_cast<uint8_t*>(p.o) + ((size_t)(b * p.Hq + hq) * p.Sq + hb * 16) * ROW_BYTES;
 #pragma unroll
         for (int q = lane; q < 16 * CHUNKS; q += 32) {
@@ -974,10 +1117,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bars + 8u * (L::B_IFULL + e), 1);                 // load-warp lane 0
       mbar_init(bars + 8u * (L::B_IEMPTY + e), 1 + QT * BM);      // MMA thread + softmax threads
     }
+    for (int sl = 0; sl < L::S_SLOTS; ++sl) mbar_init(bars + 8u * (L::B_STILE + sl), 1);
     for (int t = 0; t < QT; ++t) {
-      mbar_init(bars + 8u * (L::B_STILE + t), 1);
       mbar_init(bars + 8u * (L::B_PREADY + t), BM);
       mbar_init(bars + 8u * (L::B_ODONE + t), 1);
+      mbar_init(bars + 8u * (L::B_OPV + t), 1);
     }
     mbar_init(bars + 8u * L::B_DRAIN, 1);
     abort_flag[0] = 0;
@@ -1002,22 +1146,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   if constexpr (MODE == MASK_CUSTOM) grid_dependency_wait();
 
   // Register rebalancing: the load / MMA warpgroup (warps 0-3) needs few registers, the
-  // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 88 + 256 x 208 exactly.
+  // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 88 + 256 x 208 exactly
+  // (d = 128); 128 x 96 + 256 x 200 (d = 64).
   // Each setmaxnreg sits in the same branch as the code it budgets for.
   if (warp < 4) {
-    setmaxnreg_dec<REGS_LOADMMA>();
+    setmaxnreg_dec<L::REGS_LOADMMA>();
     if (warp == 0) {
       load_role<D, BF16, MODE>(p, base, gbase, abort_flag, lane);
     } else if (warp == 1) {
       mma_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem, lane);
     }
   } else {
-    setmaxnreg_inc<REGS_SOFTMAX>();
+    setmaxnreg_inc<L::REGS_SOFTMAX>();
     softmax_role<D, BF16, MODE>(p, base, gbase, abort_flag, tmem, (warp - 4) >> 2, warp & 3, lane);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && p.dynamic) {
+    // this CTA takes no more units; the last CTA to get here resets the queue for the next launch
+    unsigned int* q = g_sched + 2 * p.status_slot;
+    __threadfence();
+    if (atomicAdd(q + 1, 1u) == gridDim.x - 1) {
+      __threadfence();
+      atomicExch(q, 0u);
+      atomicExch(q + 1, 0u);
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -1090,24 +1245,18 @@ __global__ void __launch_bounds__(BM) mask_prepass_kernel(const uint32_t* __rest
   }
 }
 
-// Compaction of one mask row block (one CTA per block, 256 threads): which 16-row blocks
-// hold a kept entry, their ascending list (the compacted slots, -1 past its end), and the
-// (compacted tile, key tile) flags as the OR over the tile's eight slots.  Shared memory:
-// nslots (>= nqt * 8 >= nr16) slot entries and nr16 bytes of liveness.
-__global__ void __launch_bounds__(256) mask_compact_kernel(const uint8_t* __restrict__ flags16,
-                                                          uint8_t* __restrict__ live, int* __restrict__ rowmap,
-                                                          uint8_t* __restrict__ tflags, int nr16, int nkt,
-                                                          int nqt, int nslots) {
-  grid_launch_dependents();  // the attention grid may start its set-up; it waits for our output
-  grid_dependency_wait();    // launched as a dependent of the pre-pass: its flags are complete
-  extern __shared__ int cmp_smem[];
-  int* slot_s = cmp_smem;                                             // nslots
-  uint8_t* live_s = reinterpret_cast<uint8_t*>(cmp_smem + nslots);    // nr16
-  __shared__ int warp_tot[8];
+// Compaction of mask row block mb by the whole CTA (blockDim.x a multiple of 32, <= 1024)
+// from its (16-row block, key tile) flags f [nr16][nkt] (global or shared memory): which
+// 16-row blocks hold a kept entry, their ascending list (the compacted slots, -1 past its end),
+// and the (compacted tile, key tile) flags as the OR over the tile's eight slots.  slot_s
+// (nslots >= nqt * 8 >= nr16 ints) and live_s (nr16 bytes) are shared-memory scratch.
+__device__ __forceinline__ void compact_rows(const uint8_t* f, uint8_t* __restrict__ live, int* __restrict__ rowmap,
+                                             uint8_t* __restrict__ tflags, int mb, int nr16, int nkt, int nqt,
+                                             int nslots, int* slot_s, uint8_t* live_s) {
+  __shared__ int warp_tot[32];
   __shared__ int carry_s;
-  const int mb = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint8_t* f = flags16 + (size_t)mb * nr16 * nkt;
-  for (int r = tid; r < nr16; r += 256) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x, nwarp = nthr >> 5;
+  for (int r = tid; r < nr16; r += nthr) {
     uint32_t any = 0;
     for (int kt = 0; kt < nkt; ++kt) any |= f[(size_t)r * nkt + kt];
     live_s[r] = any ? 1 : 0;
@@ -1115,8 +1264,8 @@ __global__ void __launch_bounds__(256) mask_compact_kernel(const uint8_t* __rest
   }
   if (tid == 0) carry_s = 0;
   __syncthreads();
-  // ascending list of the live blocks: a block-wide exclusive scan, 256 blocks per round
-  for (int base = 0; base < nr16; base += 256) {
+  // ascending list of the live blocks: a block-wide exclusive scan, nthr blocks per round
+  for (int base = 0; base < nr16; base += nthr) {
     const int r = base + tid;
     const bool v = r < nr16 && live_s[r];
     const uint32_t bal = __ballot_sync(0xffffffffu, v);
@@ -1128,23 +1277,38 @@ __global__ void __launch_bounds__(256) mask_compact_kernel(const uint8_t* __rest
     __syncthreads();
     if (tid == 0) {
       int tot = 0;
-      for (int w = 0; w < 8; ++w) tot += warp_tot[w];
+      for (int w = 0; w < nwarp; ++w) tot += warp_tot[w];
       carry_s += tot;
     }
     __syncthreads();
   }
   const int c = carry_s;
-  for (int sl = tid; sl < nslots; sl += 256) {
+  for (int sl = tid; sl < nslots; sl += nthr) {
     if (sl >= c) slot_s[sl] = -1;
     rowmap[(size_t)mb * nslots + sl] = sl < c ? slot_s[sl] : -1;
   }
   __syncthreads();
-  for (int idx = tid; idx < nqt * nkt; idx += 256) {
+  for (int idx = tid; idx < nqt * nkt; idx += nthr) {
     const int ct = idx / nkt, kt = idx % nkt;
     uint32_t any = 0;
     for (int sl = ct * 8; sl < ct * 8 + 8 && sl < c; ++sl) any |= f[(size_t)slot_s[sl] * nkt + kt];
     tflags[(size_t)mb * nqt * nkt + idx] = any ? 1 : 0;
   }
+}
+
+// Compaction of one mask row block (one CTA per block, 256 threads) from the pre-pass's flags.
+// Shared memory: nslots (>= nqt * 8 >= nr16) slot entries and nr16 bytes of liveness.
+__global__ void __launch_bounds__(256) mask_compact_kernel(const uint8_t* __restrict__ flags16,
+                                                          uint8_t* __restrict__ live, int* __restrict__ rowmap,
+                                                          uint8_t* __restrict__ tflags, int nr16, int nkt,
+                                                          int nqt, int nslots) {
+  grid_launch_dependents();  // the attention grid may start its set-up; it waits for our output
+  grid_dependency_wait();    // launched as a dependent of the pre-pass: its flags are complete
+  extern __shared__ int cmp_smem[];
+  int* slot_s = cmp_smem;                                             // nslots
+  uint8_t* live_s = reinterpret_cast<uint8_t*>(cmp_smem + nslots);    // nr16
+  const int mb = blockIdx.x;
+  compact_rows(flags16 + (size_t)mb * nr16 * nkt, live, rowmap, tflags, mb, nr16, nkt, nqt, nslots, slot_s, live_s);
 }
 
 }  // namespace attn
@@ -1384,6 +1548,9 @@ int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream
   const long long blocks = (long long)nmb * p.nqt * p.nkt;
   if (blocks > INT_MAX) return ATTN_ERR_INVALID;
   const int nslots = p.nqb * 16;
+  p.tflags = tflags;
+  p.rowmap = rowmap;
+  p.live = live;
   const size_t cmp_smem = (size_t)nslots * 4 + (size_t)p.nr16;
   if (cmp_smem > 227 * 1024) return ATTN_ERR_UNSUPPORTED;
   if (cmp_smem > 48 * 1024) {
@@ -1413,9 +1580,6 @@ int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream
                            p.nqt, nslots) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
-  p.tflags = tflags;
-  p.rowmap = rowmap;
-  p.live = live;
   int rc = make_mask_map(&p.tm_m, words4, 4 * p.nkt, p.Sq, nmb, 16);
   return rc != ATTN_OK ? rc : make_mask_map(&p.tm_m256, words4, 4 * p.nkt, p.Sq, nmb, UNIT_ROWS);
 }
@@ -1557,6 +1721,9 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // entry of a stream it has not seen: such a stream reports through the shared slot 0.
   StreamState* ss = stream_state(dev, a.stream, !noalloc);
   p.status_slot = ss ? ss->slot : 0;
+  // A stream with a slot of its own takes units from its work queue; the shared slot 0 may
+  // serve launches on several streams at once, so those keep the fixed walk.
+  p.dynamic = p.status_slot != 0 ? 1 : 0;
   const auto run = [&]() {
     if (a.d == 64)
       return bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);

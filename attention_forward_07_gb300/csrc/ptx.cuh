@@ -181,6 +181,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// Named barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Warpgroup register rebalancing (all four warps of a warpgroup execute the same one).
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
