@@ -181,6 +181,10 @@ struct Params {
   int inject;
   int status_slot;  // index into g_attn_status of the stream this launch runs on
   int dynamic;      // 1: units are taken from the slot's work queue (g_sched), else a fixed walk
+  // Variable-length batches with the work queue: the (batch entry, 256-row block) pairs in the
+  // order they are handed out, most key tiles first (written by unit_order_kernel); the query
+  // heads of a pair follow one another.  NULL: the order decode_unit computes.
+  const int* order;
   float scale_log2;
   uint32_t timeout_us;  // longest barrier wait (microseconds; 32 bits keep it in one register)
 };
@@ -257,7 +261,13 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 // and CTAs that finish early take the next unit, which keeps the load balanced.
 __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, int& b, int& hq,
                                             int& qb) {
-  if (causal && p.dynamic) {
+  if (p.order) {
+    const int pi = u / p.Hq;
+    const int pair = __ldg(p.order + pi);
+    b = pair / p.nqb;
+    qb = pair - b * p.nqb;
+    hq = u - pi * p.Hq;
+  } else if (causal && p.dynamic) {
     const int G = p.B * p.Hkv;
     int hi = p.nqb, base = 0;
     while (true) {
@@ -1143,7 +1153,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   // Custom masks: the set-up above overlapped the mask kernels (dependent launch); their
   // words, flags and slot lists are read only after this point.
-  if constexpr (MODE == MASK_CUSTOM) grid_dependency_wait();
+  // Custom masks and variable-length work orders: the set-up above overlapped the kernels
+  // that write them (dependent launch); they are read only after this point.
+  if (MODE == MASK_CUSTOM || p.order) grid_dependency_wait();
 
   // Register rebalancing: the load / MMA warpgroup (warps 0-3) needs few registers, the
   // softmax warpgroups hold a 128-score row each.  384 x 168 = 128 x 88 + 256 x 208 exactly
@@ -1309,6 +1321,68 @@ __global__ void __launch_bounds__(256) mask_compact_kernel(const uint8_t* __rest
   uint8_t* live_s = reinterpret_cast<uint8_t*>(cmp_smem + nslots);    // nr16
   const int mb = blockIdx.x;
   compact_rows(flags16 + (size_t)mb * nr16 * nkt, live, rowmap, tflags, mb, nr16, nkt, nqt, nslots, slot_s, live_s);
+}
+
+// Key tiles the two Q tiles of work unit (b, any head, 256-row block qb) compute -- the same
+// bounds the load warp uses (per-entry lengths, bottom-right alignment, band).
+__device__ __forceinline__ int unit_weight(const Params& p, int b, int qb) {
+  int sq, sk, qoff, koff;
+  unit_span(p, b, sq, sk, qoff, koff);
+  const int off = sk - sq;
+  int w = 0;
+#pragma unroll
+  for (int t = 0; t < QT; ++t) {
+    const int r0 = qb * UNIT_ROWS + t * BM;
+    const int r1 = min(r0 + BM - 1, sq - 1);
+    const int rf = p.er >= 0 ? max(r0, -off - p.er) : r0;
+    const int klo = key_lo(p, rf, off), khi = key_hi(p, r1, off, sk);
+    if (r0 < sq && rf <= r1 && khi > klo) w += (khi - 1) / BN - klo / BN + 1;
+  }
+  return w;
+}
+
+// Work order of a variable-length batch (one CTA): the (batch entry, 256-row block) pairs
+// sorted by the key tiles they compute, most first (a counting sort over the weights
+// 0 .. 2 * nkt), so the work queue hands out the longest units first whatever the entries'
+// lengths.  Pairs of equal weight come in no particular order (each unit's result does not
+// depend on when it runs).  Shared memory: nbins = 2 * nkt + 1 counters.
+constexpr int ORDER_THREADS = 1024;
+__global__ void __launch_bounds__(ORDER_THREADS) unit_order_kernel(const Params p, int* __restrict__ order) {
+  grid_launch_dependents();  // the attention grid may start its set-up; it waits for our output
+  extern __shared__ int bins[];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nbins = 2 * p.nkt + 1, npairs = p.B * p.nqb;
+  for (int i = tid; i < nbins; i += ORDER_THREADS) bins[i] = 0;
+  __syncthreads();
+  for (int pr = tid; pr < npairs; pr += ORDER_THREADS) {
+    const int b = pr / p.nqb;
+    atomicAdd(&bins[nbins - 1 - unit_weight(p, b, pr - b * p.nqb)], 1);
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // exclusive scan of the bins by one warp: each lane a contiguous chunk, then the lanes'
+    // totals scanned with shuffles
+    const int per = (nbins + 31) / 32, lo = lane * per, hi = min(lo + per, nbins);
+    int tot = 0;
+    for (int i = lo; i < hi; ++i) tot += bins[i];
+    int incl = tot;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += x;
+    }
+    int run = incl - tot;
+    for (int i = lo; i < hi; ++i) {
+      const int c = bins[i];
+      bins[i] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int pr = tid; pr < npairs; pr += ORDER_THREADS) {
+    const int b = pr / p.nqb;
+    order[atomicAdd(&bins[nbins - 1 - unit_weight(p, b, pr - b * p.nqb)], 1)] = pr;
+  }
 }
 
 }  // namespace attn
@@ -1585,7 +1659,7 @@ int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream
 }
 
 template <int D, bool BF16, int MODE>
-int launch(const Params& p, int grid, cudaStream_t st, int dev) {
+int launch(const Params& p, int grid, cudaStream_t st, int dev, bool dependent) {
   using L = Layout<D, MODE>;
   auto kern = attn_fwd_kernel<D, BF16, MODE>;
   static std::atomic<unsigned long long> attr_set{0};  // bit per device
@@ -1596,8 +1670,9 @@ int launch(const Params& p, int grid, cudaStream_t st, int dev) {
       return ATTN_ERR_CUDA;
     attr_set.fetch_or(bit);
   }
-  if constexpr (MODE == MASK_CUSTOM) {
-    // Launched as a programmatic dependent of the mask compaction just enqueued on `st`.
+  if (dependent) {
+    // Launched as a programmatic dependent of the kernel just enqueued on `st` (the mask
+    // compaction or the work order), whose output it waits for with griddepcontrol.wait.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(NTHREADS);
@@ -1615,12 +1690,12 @@ int launch(const Params& p, int grid, cudaStream_t st, int dev) {
 }
 
 template <int D, bool BF16>
-int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev) {
+int launch_mode(const Params& p, int mode, int grid, cudaStream_t st, int dev, bool dependent) {
   switch (mode) {
-    case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st, dev);
-    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st, dev);
-    case MASK_BAND: return launch<D, BF16, MASK_BAND>(p, grid, st, dev);
-    default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st, dev);
+    case MASK_NONE: return launch<D, BF16, MASK_NONE>(p, grid, st, dev, dependent);
+    case MASK_CAUSAL: return launch<D, BF16, MASK_CAUSAL>(p, grid, st, dev, dependent);
+    case MASK_BAND: return launch<D, BF16, MASK_BAND>(p, grid, st, dev, dependent);
+    default: return launch<D, BF16, MASK_CUSTOM>(p, grid, st, dev, dependent);
   }
 }
 
@@ -1724,16 +1799,25 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // A stream with a slot of its own takes units from its work queue; the shared slot 0 may
   // serve launches on several streams at once, so those keep the fixed walk.
   p.dynamic = p.status_slot != 0 ? 1 : 0;
+  // Variable-length batches with the work queue get a work order, longest units first.
+  const bool varlen = packed || a.seqlens_q || a.seqlens_k;
+  const bool with_order = varlen && p.dynamic && 2ll * p.nkt + 1 <= 8192;
+  const bool custom = mode == MASK_CUSTOM;
   const auto run = [&]() {
+    const bool dep = custom || with_order;
     if (a.d == 64)
-      return bf16 ? launch_mode<64, true>(p, mode, grid, st, dev) : launch_mode<64, false>(p, mode, grid, st, dev);
-    return bf16 ? launch_mode<128, true>(p, mode, grid, st, dev) : launch_mode<128, false>(p, mode, grid, st, dev);
+      return bf16 ? launch_mode<64, true>(p, mode, grid, st, dev, dep) : launch_mode<64, false>(p, mode, grid, st, dev, dep);
+    return bf16 ? launch_mode<128, true>(p, mode, grid, st, dev, dep)
+                : launch_mode<128, false>(p, mode, grid, st, dev, dep);
   };
-  if (mode != MASK_CUSTOM) return run();
-  // Custom masks: the mask kernels write into scratch that the attention kernel reads.
-  const size_t need = MaskScratch((long long)a.B * p.mask_heads, a.Sq, a.Sk).total();
+  if (!custom && !with_order) return run();
+  // Scratch in the stream's workspace: the mask kernels' output, then the work order.
+  const size_t mask_bytes = custom ? MaskScratch((long long)a.B * p.mask_heads, a.Sq, a.Sk).total() : 0;
+  const size_t order_off = (mask_bytes + 255) & ~(size_t)255;
+  const size_t need = order_off + (with_order ? (size_t)a.B * p.nqb * sizeof(int) : 0);
   if (noalloc) {
-    // the fixed array: reject what does not fit before anything is launched
+    // the fixed array (attn_fwd_noalloc takes no variable lengths): reject what does not fit
+    // before anything is launched
     if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_INVALID;
     void* scratch = nullptr;
     if ((rc = noalloc_scratch_address(&scratch)) != ATTN_OK) return rc;
@@ -1742,7 +1826,14 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   }
   std::lock_guard<std::mutex> lk(ss->m);
   if ((rc = ensure_workspace(*ss, need, st)) != ATTN_OK) return rc;
-  if ((rc = prepare_mask(p, a.mask_bits, ss->ws, st, dev)) != ATTN_OK) return rc;
+  if (with_order) {
+    // first, as a plain launch: the mask kernels (if any) start after it has finished
+    int* order = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ss->ws) + order_off);
+    unit_order_kernel<<<1, ORDER_THREADS, (2 * p.nkt + 1) * sizeof(int), st>>>(p, order);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    p.order = order;
+  }
+  if (custom && (rc = prepare_mask(p, a.mask_bits, ss->ws, st, dev)) != ATTN_OK) return rc;
   return run();
 }
 

@@ -130,6 +130,41 @@ class Workload:
         return q, k, v, bits
 
 
+@dataclass(frozen=True)
+class PackedWorkload:
+    """A packed variable-length batch (this library's extension of the pages' prefill set):
+    entries of the given lengths laid out head-major, q / o [Hq, total, d], k / v
+    [Hkv, total, d], entry b at rows cu[b] .. cu[b+1]-1, queries and keys of equal length."""
+    name: str
+    lengths: tuple
+    Hq: int
+    Hkv: int
+    d: int
+    dtype: int
+    causal: bool
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.d)))
+
+    @property
+    def total(self) -> int:
+        return int(sum(self.lengths))
+
+    def flops(self) -> float:
+        """Sum over entries of 4*Hq*s^2*d, halved for causal (the prefill formula per entry)."""
+        f = sum(4.0 * self.Hq * s * s * self.d for s in self.lengths)
+        return f / 2 if self.causal else f
+
+    def cu_seqlens(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lengths)]).astype(np.int32)
+
+    def make(self, seed):
+        """q [Hq, total, d], k and v [Hkv, total, d] (N(0,1), rounded), cu_seqlens int32 [B+1]."""
+        q, k, v = qkv(1, self.Hq, self.Hkv, self.total, self.d, self.dtype, seed)
+        return q[0].contiguous(), k[0].contiguous(), v[0].contiguous(), self.cu_seqlens()
+
+
 def _prefill(name, S, Hq, Hkv, causal):
     return Workload(name, 32768 // S, Hq, Hkv, S, 128, BF16, causal, "none")
 
@@ -145,3 +180,9 @@ for _S in (4096, 8192, 16384, 32768):
     for _hkv in (4, 8):
         WORKLOADS[f"gqa{_hkv}_causal_S{_S}"] = _prefill(f"gqa{_hkv}_causal_S{_S}", _S, 32, _hkv, True)
         WORKLOADS[f"gqa{_hkv}_S{_S}"] = _prefill(f"gqa{_hkv}_S{_S}", _S, 32, _hkv, False)
+
+# Packed variable-length causal prefill, 8 entries of 1k-16k rows (53248 in all), GQA 32/8.
+PACKED_WORKLOADS = {
+    "packed_causal_gqa8": PackedWorkload("packed_causal_gqa8", (16384, 1024, 8192, 2048, 12288, 4096, 3072, 6144),
+                                         32, 8, 128, BF16, True),
+}

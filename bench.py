@@ -429,6 +429,30 @@ def run_sweep(af, torch, dev, warmup=10, timed=50):
         rows[name] = row
         del t, qd, kd, vd, md, o, lse
         torch.cuda.empty_cache()
+    for name, pw in inp.PACKED_WORKLOADS.items():
+        # this library's extension: a packed variable-length batch, through attn_fwd_packed
+        q, k, v, cu = pw.make(1000 + len(pw.lengths))
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        cud = torch.from_numpy(cu).to(dev)
+        o = torch.empty_like(qd)
+        lse = torch.empty((pw.Hq, pw.total), dtype=torch.float32, device=dev)
+        mx = max(pw.lengths)
+
+        def pstep():
+            af.attn_fwd_packed(qd, kd, vd, o, cud, cud, mx, mx, lse=lse, causal=pw.causal, scale=pw.scale)
+
+        ms = launch_times(torch, dev, pstep, warmup, timed, None)
+        af.attn_check()
+        med = statistics.median(ms)
+        p_tensor, _, _ = peaks()
+        ach = pw.flops() / (med / 1e3) / 1e12
+        rows[name] = {"ms_median": med, "ms_mean": statistics.mean(ms), "value": ach, "unit": "TFLOPS",
+                      "bound": "tensor", "achieved": ach, "achieved_unit": "TFLOP/s", "frac": ach / p_tensor,
+                      "lengths": list(pw.lengths), "Hq": pw.Hq, "Hkv": pw.Hkv, "d": pw.d, "causal": pw.causal,
+                      "extension": "packed variable-length batch (not one of the pages' configurations)",
+                      "launches": timed * 2}
+        del qd, kd, vd, cud, o, lse
+        torch.cuda.empty_cache()
     return rows
 
 

@@ -161,3 +161,30 @@ def test_prefill_every_row_mha_causal_S4096():
         rows = np.arange(b * per_b, (b + 1) * per_b, dtype=np.int64)
         o_ref, lse_ref = oracle_rows(q, k, v, bits, w.causal, w.scale, w.dtype, rows)
         assert_close(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, f"{name} b={b}")
+
+
+def test_packed_workload_sampled_parity():
+    """The packed variable-length causal batch of the benchmark's sweep (8 entries of 1k-16k
+    rows, GQA 32/8), launched as bench.py launches it, checked entry by entry against the
+    oracle on a stratified row sample of every head."""
+    import attention_forward_07_gb300 as af
+    pw = inp.PACKED_WORKLOADS["packed_causal_gqa8"]
+    q, k, v, cu = pw.make(1000 + len(pw.lengths))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((pw.Hq, pw.total), float("nan"), dtype=torch.float32, device="cuda")
+    mx = max(pw.lengths)
+    af.attn_fwd_packed(qd, kd, vd, o, torch.from_numpy(cu).cuda(), torch.from_numpy(cu).cuda(), mx, mx, lse=lse,
+                       causal=True, scale=pw.scale)
+    af.attn_check()
+    og = o.float().cpu().numpy().astype(np.float64)
+    lg = lse.cpu().numpy().astype(np.float64)
+    for b, s in enumerate(pw.lengths):
+        lo = int(cu[b])
+        qb = q[:, lo:lo + s].unsqueeze(0).contiguous()
+        kb = k[:, lo:lo + s].unsqueeze(0).contiguous()
+        vb = v[:, lo:lo + s].unsqueeze(0).contiguous()
+        rows = stratified_rows(1, pw.Hq, s, seed=s)
+        o_ref, lse_ref = oracle_rows(qb, kb, vb, None, True, pw.scale, pw.dtype, rows)
+        h, i = rows // s, rows % s
+        assert_close(og[h, lo + i], lg[h, lo + i], o_ref, lse_ref, f"packed entry {b} (length {s})")
