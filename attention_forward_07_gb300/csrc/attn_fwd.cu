@@ -22,8 +22,13 @@
 //                exp2, row sum, write P back into TMEM as fp16/bf16, rescale the O row
 //                when the running max grew (the correction step), and at the end of the
 //                unit normalise O, store it and the LSE.
-// Work unit = (batch, query head, 256-row block); units are dealt to CTAs in a fixed
-// snake order; for causal masks the heaviest blocks (most key tiles) come first.
+// Work unit = (batch, query head, 256-row block).  Units of equal size and variable-length
+// batches come from a work queue per stream (an atomic counter the last CTA resets), the
+// latter in a longest-first order a one-CTA counting sort writes; causal units of uniform
+// lengths and custom-mask units are dealt in a fixed snake order, the heaviest blocks (most
+// key tiles) first.
+// d = 64 keeps three S slots in TMEM shared by the two Q tiles, so a Q tile's next Q.K^T runs
+// while its softmax works on the current one.
 // Custom masks go through two small kernels first: the pre-pass ANDs the caller's words
 // with the causal / window / length bounds into whole-tile words and flags each (16-row
 // block, key tile) pair that keeps anything; the compaction lists the 16-row blocks that
@@ -249,16 +254,12 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 }
 
 // Unit -> (batch, query head, 256-row block).
-// Not causal: consecutive units walk the blocks and the query heads of one K/V head, so the
+// Variable-length batches (work queue): the pairs of p.order, longest first, the query heads
+// of a pair adjacent.
+// Causal: block index descending (the longest units first), the heads of a block adjacent; the
+// fixed snake walk deals them so that every CTA's total is close to the mean.
+// Otherwise: consecutive units walk the blocks and the query heads of one K/V head, so the
 // CTAs running at one time share K/V through L2.
-// Causal with the fixed walk: block index descending (the longest units first), the heads of
-// a block adjacent.
-// Causal with the work queue: bands of blocks from the longest down, each band half of the
-// blocks left (at least one): [nqb - w0, nqb), then w1 = ceil(rest / 2) below it, and so on,
-// so the last units handed out are the shortest.  Inside a band the units go K/V head by K/V
-// head (b, hkv), and for one K/V head the band's blocks longest first with the g query heads
-// of a block adjacent: the CTAs running at one time read a few K/V heads, which stay in L2,
-// and CTAs that finish early take the next unit, which keeps the load balanced.
 __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, int& b, int& hq,
                                             int& qb) {
   if (p.order) {
@@ -267,23 +268,6 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
     b = pair / p.nqb;
     qb = pair - b * p.nqb;
     hq = u - pi * p.Hq;
-  } else if (causal && p.dynamic) {
-    const int G = p.B * p.Hkv;
-    int hi = p.nqb, base = 0;
-    while (true) {
-      const int w = (hi + 1) / 2;
-      const int n = G * p.g * w;
-      if (u < base + n || hi - w <= 0) {
-        const int v = u - base, per_group = p.g * w;
-        const int grp = v / per_group, r = v % per_group;
-        qb = hi - 1 - r / p.g;
-        b = grp / p.Hkv;
-        hq = (grp % p.Hkv) * p.g + r % p.g;
-        return;
-      }
-      base += n;
-      hi -= w;
-    }
   } else if (causal) {
     const int bh = u % (p.B * p.Hq);
     qb = p.nqb - 1 - u / (p.B * p.Hq);
@@ -298,15 +282,6 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
     b = bk / p.Hkv;
     hq = hkv * p.g + member;
   }
-}
-
-// The load warp's next unit (the same value in every lane), or -1 when none is left.
-__device__ __forceinline__ int next_unit(const Params& p, int k, int lane) {
-  if (!p.dynamic) return unit_at(k, p.num_units);
-  unsigned int x = 0;
-  if (lane == 0) x = atomicAdd(&g_sched[2 * p.status_slot], 1u);
-  x = __shfl_sync(0xffffffffu, x, 0);
-  return x < (unsigned int)p.num_units ? (int)x : -1;
 }
 
 // Query / key lengths of batch entry b and, for packed layouts, its first query and key row
@@ -378,8 +353,19 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
   uint32_t ipend = 0, ipend_par = 0;  // descriptor slots with a mask-word load issued
   bool inject = p.inject != 0;
 
+  // The work queue: lane 0 fetches the index of the unit after the current one as the current
+  // one starts, so the atomic's round trip to L2 overlaps the current unit's loads.
+  unsigned int q_next = 0;
+  if (p.dynamic && lane == 0) q_next = atomicAdd(&g_sched[2 * p.status_slot], 1u);
   for (int k = 0;; ++k) {
-    const int u = next_unit(p, k, lane);
+    int u;
+    if (p.dynamic) {
+      const unsigned int x = __shfl_sync(0xffffffffu, q_next, 0);
+      u = x < (unsigned int)p.num_units ? (int)x : -1;
+      if (u >= 0 && lane == 0) q_next = atomicAdd(&g_sched[2 * p.status_slot], 1u);
+    } else {
+      u = unit_at(k, p.num_units);
+    }
     if (u < 0) {
       // no unit left: an exit descriptor releases the MMA warp and the softmax warpgroups
       if (!bwait_warp(bars + 8u * (L::B_IEMPTY + ie), ie_par, abort_flag, to)) goto drain;
@@ -1796,12 +1782,15 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // entry of a stream it has not seen: such a stream reports through the shared slot 0.
   StreamState* ss = stream_state(dev, a.stream, !noalloc);
   p.status_slot = ss ? ss->slot : 0;
-  // A stream with a slot of its own takes units from its work queue; the shared slot 0 may
-  // serve launches on several streams at once, so those keep the fixed walk.
-  p.dynamic = p.status_slot != 0 ? 1 : 0;
+  // Units of equal size (no right bound on the keys, no custom mask) and variable-length
+  // batches are taken from the stream's work queue, so CTAs that finish early take more.
+  // Causal units of uniform lengths and custom-mask units keep the fixed snake walk over the
+  // longest-first order, which balances them better (measured).  The shared slot 0 may serve
+  // launches on several streams at once, so those keep the fixed walk too.
+  const bool varlen_batch = packed || a.seqlens_q || a.seqlens_k;
+  p.dynamic = (p.status_slot != 0 && (varlen_batch || (!a.mask_bits && p.er < 0))) ? 1 : 0;
   // Variable-length batches with the work queue get a work order, longest units first.
-  const bool varlen = packed || a.seqlens_q || a.seqlens_k;
-  const bool with_order = varlen && p.dynamic && 2ll * p.nkt + 1 <= 8192;
+  const bool with_order = varlen_batch && p.dynamic && 2ll * p.nkt + 1 <= 8192;
   const bool custom = mode == MASK_CUSTOM;
   const auto run = [&]() {
     const bool dep = custom || with_order;

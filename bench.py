@@ -293,13 +293,11 @@ def run_reference(args):
 # DRAM bytes (read + write) per launch from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`,
 # keyed by the sha1 of the kernel sources they were taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, per kernel
-    # source hash.  Causal GQA B=2 S=4096 was captured (132.05 MB); the default B=4 S=8192
-    # launch processes 4x the units and reads 4x the compulsory Q/K/V bytes, so its traffic
-    # is scaled by 4.  The short masked workload was captured at full size (50.95 MB).
-    "11ae5e36e185": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 4 * 132.05e6,
-                     "B2_Hq32_Hkv8_S4096_d128_causal_none": 132.05e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.95e6},
+    # dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, captured at
+    # full size (one launch, metrics-only, 1 pass) on the kernel with this source hash
+    "52638277a8b8": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1555.07e6 + 238.26e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.45e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_block90": 36.92e6 + 0.01e6},
 }
 
 
@@ -423,7 +421,7 @@ def run_sweep(af, torch, dev, warmup=10, timed=50):
         row = {"ms_median": med, "ms_mean": statistics.mean(ms), "value": w.flops() / (med / 1e3) / 1e12,
                "unit": "TFLOPS", "bound": rf["bound"], "achieved": rf["achieved"], "achieved_unit": rf["unit"],
                "frac": rf["frac"], "frac_of_mean": rf["frac"] * med / statistics.mean(ms),
-               "live_fraction": live, "launches": timed * kernels_per_step(w)}
+               "live_fraction": live, "traffic": rf["traffic"], "launches": timed * kernels_per_step(w)}
         if w.mask != "none":
             row["tiles"] = skip_counts(af, torch, dev, w, t)
         rows[name] = row
