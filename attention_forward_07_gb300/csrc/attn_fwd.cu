@@ -190,6 +190,10 @@ struct Params {
   // order they are handed out, most key tiles first (written by unit_order_kernel); the query
   // heads of a pair follow one another.  NULL: the order decode_unit computes.
   const int* order;
+  // 1 when Sq <= 128 and the GQA group size is even (no custom mask): a unit is a pair of query
+  // heads (hq, hq + 1) of one K/V head, Q tile t holding rows 0..127 of head hq + t, so both
+  // softmax warpgroups work on one stream of K/V tiles; 0: Q tile t holds rows 128 t.. of hq.
+  int pair;
   float scale_log2;
   uint32_t timeout_us;  // longest barrier wait (microseconds; 32 bits keep it in one register)
 };
@@ -260,9 +264,17 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 // fixed snake walk deals them so that every CTA's total is close to the mean.
 // Otherwise: consecutive units walk the blocks and the query heads of one K/V head, so the
 // CTAs running at one time share K/V through L2.
-__device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, int& b, int& hq,
+__device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, bool pair, int& b, int& hq,
                                             int& qb) {
-  if (p.order) {
+  if (pair) {
+    // (entry, block) pairs in the work order or in index order, then the head pairs of
+    // consecutive K/V heads (an even group size keeps a pair inside one group)
+    const int hp = p.Hq >> 1, pi = u / hp;
+    const int pr = p.order ? __ldg(p.order + pi) : pi;
+    b = pr / p.nqb;
+    qb = pr - b * p.nqb;
+    hq = 2 * (u - pi * hp);
+  } else if (p.order) {
     const int pi = u / p.Hq;
     const int pair = __ldg(p.order + pi);
     b = pair / p.nqb;
@@ -337,6 +349,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
                                           volatile int* abort_flag, int lane) {
   using L = Layout<D, MODE>;
   const bool causal = (MODE == MASK_CAUSAL) || (MODE != MASK_NONE && p.causal != 0);
+  const bool pair = MODE != MASK_CUSTOM && p.pair;  // head pairs never come with a custom mask
   const uint32_t to = p.timeout_us;
   const uint32_t bars = base + L::OFF_BAR;
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
@@ -379,7 +392,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       break;
     }
     int b, hq, qb;
-    decode_unit(u, p, causal, b, hq, qb);
+    decode_unit(u, p, causal, pair, b, hq, qb);
     const int hkv = hq / p.g;
     const int row0 = qb * UNIT_ROWS;
     const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
@@ -425,7 +438,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
 #pragma unroll
           for (int h = 0; h < L::HALVES; ++h)
             tma_load_3d(base + L::OFF_Q + qbuf * L::Q_BUF_BYTES + t * L::Q_TILE_BYTES + h * BM * 128,
-                        &p.tm_q, fb, h * 64, qoff + row0 + t * BM, qz);
+                        &p.tm_q, fb, h * 64, qoff + row0 + (pair ? 0 : t * BM), qz + (pair ? t : 0));
       }
       // this fill completes the phase the consumer waits for with parity (empty parity ^ 1)
       q_pend |= 1u << qbuf;
@@ -440,7 +453,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     int jlo[QT], jhi[QT];
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
-      const int r0 = row0 + t * BM;
+      const int r0 = row0 + (pair ? 0 : t * BM);
       const int r1 = min(r0 + BM - 1, sq - 1);
       const int rf = p.er >= 0 ? max(r0, -off - p.er) : r0;
       const int klo = key_lo(p, rf, off), khi = key_hi(p, r1, off, sk);
@@ -600,6 +613,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
   volatile InfoHdr* hdr = reinterpret_cast<volatile InfoHdr*>(gbase + L::OFF_HDR);
   constexpr uint32_t ID_QK = idesc_f16acc32(BF16, false, false, BM, BN);
   constexpr uint32_t ID_PV = idesc_f16acc32(BF16, false, true, BM, D);
+  const bool pair = MODE != MASK_CUSTOM && p.pair;
 
   uint32_t q_par = 0, ie_par = 0, kpar = 0, vpar = 0, p_par0 = 0, p_par1 = 0;  // q_par: bit per Q buffer
   int kslot = 0, vslot = 0, ie = 0;
@@ -674,7 +688,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
               }
               tc_commit_elect(bars + 8u * (L::B_STILE + new_slot));
               if (p.visited && lane == 0)
-                p.visited[((size_t)(b * p.Hq + hq) * p.nqt + (qb * QT + t)) * p.nkt + j] = 1;
+                p.visited[((size_t)(b * p.Hq + hq + (pair ? t : 0)) * p.nqt + (qb * QT + (pair ? 0 : t))) * p.nkt + j] = 1;
               __syncwarp();
             }
           } else {
@@ -763,9 +777,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     const int bh = hdr[ie].bh, qb = hdr[ie].qb;
     const int b = bh / p.Hq, hq = bh - b * p.Hq;
     const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
+    // this tile's query head and first row (head pairs: head hq + t, rows from 0)
+    const bool pair = MODE != MASK_CUSTOM && p.pair;
+    const int hq_t = hq + (pair ? t : 0);
+    const int rt = qb * UNIT_ROWS + (pair ? 0 : t * BM);
     // This thread's query row.  Custom masks: the tile holds compacted slots, 16 rows each;
     // blk_a / blk_b are the original blocks of this warp's two slots (-1: no such slot).
-    int i = qb * UNIT_ROWS + t * BM + r;
+    int i = rt + r;
     int blk_a = 0, blk_b = 0;
     bool live_a = true, live_b = true;  // this warp's own two 16-row blocks keep something
     const int hb0 = (qb * UNIT_ROWS + t * BM + quarter * 32) / 16;
@@ -976,8 +994,8 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
         }
       }
       __syncwarp();
-      const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;  // this warp's first row
-      uint8_t* obh = reinterpret_cast<uint8_t*>(p.o) + q_row_base(p, b, hq, qoff) * ROW_BYTES;
+      const int row0w = rt + quarter * 32;  // this warp's first row
+      uint8_t* obh = reinterpret_cast<uint8_t*>(p.o) + q_row_base(p, b, hq_t, qoff) * ROW_BYTES;
       constexpr int ROWS_PER_STORE = 32 / CHUNKS;
 #pragma unroll
       for (int kk = 0; kk < 32 / ROWS_PER_STORE; ++kk) {
@@ -1000,8 +1018,8 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       // Same scheme through the warp's own 4 KiB slice, one 64-column half of d per pass:
       // each store instruction then writes four whole 128-byte segments of O.
       uint8_t* stage = gbase + L::OFF_STAGE + (t * 4 + quarter) * (32 * 128);
-      const int row0w = qb * UNIT_ROWS + t * BM + quarter * 32;
-      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (q_row_base(p, b, hq, qoff) + row0w) * (D * 2);
+      const int row0w = rt + quarter * 32;
+      uint8_t* obase = reinterpret_cast<uint8_t*>(p.o) + (q_row_base(p, b, hq_t, qoff) + row0w) * (D * 2);
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
 #pragma unroll
@@ -1034,7 +1052,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
         __syncwarp();  // the slice is rewritten by the next half
       }
     } else {
-    OutT* orow = reinterpret_cast<OutT*>(p.o) + (q_row_base(p, b, hq, qoff) + (row_ok ? i : 0)) * D;
+    OutT* orow = reinterpret_cast<OutT*>(p.o) + (q_row_base(p, b, hq_t, qoff) + (row_ok ? i : 0)) * D;
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch) {
       uint32_t ob[16];
@@ -1057,7 +1075,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
     if (L::STAGE_O && lane == 0) mbar_arrive(bars + 8u * (L::B_QEMPTY + (k % L::QBUF)));
     }
     if (row_ok && p.lse)
-      p.lse[q_row_base(p, b, hq, qoff) + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+      p.lse[q_row_base(p, b, hq_t, qoff) + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
     if constexpr (MODE == MASK_CUSTOM) {
       // The unit also owns the 16-row blocks of its original rows; those with nothing kept
       // were left out of the compacted list: O = 0 and LSE = -inf there, this warp's two
@@ -1318,7 +1336,7 @@ __device__ __forceinline__ int unit_weight(const Params& p, int b, int qb) {
   int w = 0;
 #pragma unroll
   for (int t = 0; t < QT; ++t) {
-    const int r0 = qb * UNIT_ROWS + t * BM;
+    const int r0 = qb * UNIT_ROWS + (p.pair ? 0 : t * BM);
     const int r1 = min(r0 + BM - 1, sq - 1);
     const int rf = p.er >= 0 ? max(r0, -off - p.er) : r0;
     const int klo = key_lo(p, rf, off), khi = key_hi(p, r1, off, sk);
@@ -1760,6 +1778,10 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   p.nr16 = (Sq + 15) / 16;
   p.W = (Sk + 31) / 32;
   p.num_units = a.B * a.Hq * (int)nqb;
+  // GQA head pairs when one Q tile holds a whole entry's queries (no custom mask: its
+  // compaction works on the rows of one head)
+  p.pair = (Sq <= BM && (a.Hq / a.Hkv) % 2 == 0 && !a.mask_bits) ? 1 : 0;
+  if (p.pair) p.num_units = a.B * (a.Hq / 2);
   p.wl = a.window_left;
   p.er = a.causal ? 0 : a.window_right;  // causal: nothing right of the aligned position
   p.mask_heads = (a.mask_bits && a.mask_per_head) ? a.Hq : 1;

@@ -43,6 +43,11 @@ CASES = [
     (2, 2, 2, 700, 900, 128, inp.BF16, True, -1, -1, "sparse"),
     (1, 4, 4, 333, 333, 64, inp.F16, True, 90, -1, "sparse_head"),
     (2, 2, 1, 1100, 1100, 128, inp.BF16, False, 200, 100, "sparse"),
+    # at most 128 queries and an even group size: a unit pairs two query heads of a K/V head
+    (2, 8, 2, 100, 700, 128, inp.BF16, True, -1, -1, None),
+    (1, 4, 1, 128, 300, 64, inp.F16, False, -1, -1, None),
+    (2, 8, 4, 1, 513, 128, inp.BF16, True, 50, -1, None),
+    (3, 6, 3, 77, 77, 64, inp.BF16, True, -1, -1, None),
 ]
 
 
@@ -91,6 +96,7 @@ def test_ex_defaults_are_attn_fwd():
 VARLEN_CASES = [
     # B, Hq, Hkv, Sq, Sk, d, dtype, causal, wl, wr, mask
     (4, 2, 1, 300, 300, 128, inp.BF16, True, -1, -1, None),
+    (4, 8, 2, 120, 640, 128, inp.BF16, True, -1, -1, None),      # head pairs, per-entry lengths
     (4, 4, 2, 257, 520, 64, inp.F16, False, -1, -1, None),
     (3, 2, 2, 384, 700, 128, inp.F16, False, 90, 20, None),
     (4, 2, 1, 260, 400, 64, inp.BF16, True, -1, -1, "shared"),
@@ -180,6 +186,7 @@ PACKED_CASES = [
     (4, 2, 128, inp.BF16, True, -1, -1, [300, 0, 129, 512], [300, 77, 400, 512]),
     (2, 2, 64, inp.F16, False, -1, -1, [1, 256, 333], [700, 256, 333]),
     (4, 1, 64, inp.F16, True, 100, -1, [200, 450, 17, 256, 90], [200, 900, 17, 300, 1]),
+    (8, 2, 128, inp.BF16, True, -1, -1, [100, 1, 128, 64, 0, 33], [900, 1, 128, 640, 12, 33]),  # head pairs
 ]
 
 

@@ -52,6 +52,8 @@ SMALL = [
     (2, 4, 1, 512, 64, inp.F16, False, "block90"),       # tile skipping
     (1, 2, 2, 700, 64, inp.F16, True, "block90"),
     (1, 2, 2, 450, 128, inp.F16, False, "sparse"),       # most rows fully masked in some tiles
+    (2, 8, 2, 100, 128, inp.BF16, True, "none"),         # S <= 128, group 4: query-head pairs
+    (1, 4, 2, 128, 64, inp.F16, False, "none"),          # S = 128, group 2
 ]
 
 
@@ -90,12 +92,13 @@ def test_causal_equals_lower_triangular_mask():
     np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-4)
 
 
-@pytest.mark.parametrize("S,causal,mask,d", [(512, False, "block90", 64), (700, True, "block90", 64),
-                                             (1000, True, "none", 128), (384, False, "bernoulli", 128),
-                                             (600, True, "sparse", 64)])
-def test_skip_map_is_exact(S, causal, mask, d):
-    B, H = 2, 3
-    q, k, v, bits, causal, scale = _case(B, H, H, S, d, inp.F16, causal, mask, seed=S)
+@pytest.mark.parametrize("S,causal,mask,d,H,Hkv", [(512, False, "block90", 64, 3, 3), (700, True, "block90", 64, 3, 3),
+                                                     (1000, True, "none", 128, 3, 3),
+                                                     (384, False, "bernoulli", 128, 3, 3),
+                                                     (600, True, "sparse", 64, 3, 3), (100, True, "none", 128, 8, 2)])
+def test_skip_map_is_exact(S, causal, mask, d, H, Hkv):
+    B = 2
+    q, k, v, bits, causal, scale = _case(B, H, Hkv, S, d, inp.F16, causal, mask, seed=S)
     o, lse, vis = run_cuda(q, k, v, bits, causal, scale, visited=True)
     assert np.array_equal(vis, expected_visited(bits, False, B, H, S, S, causal))
     o_ref, lse_ref = oracle_full(q, k, v, bits, causal, scale, inp.F16)
