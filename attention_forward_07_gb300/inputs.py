@@ -186,3 +186,59 @@ PACKED_WORKLOADS = {
     "packed_causal_gqa8": PackedWorkload("packed_causal_gqa8", (16384, 1024, 8192, 2048, 12288, 4096, 3072, 6144),
                                          32, 8, 128, BF16, True),
 }
+
+
+@dataclass(frozen=True)
+class ExWorkload:
+    """A generalised-mode case of this library's extensions (attn_fwd_ex): Sq queries against
+    Sk keys aligned at the bottom right, an optional left window, optional per-head Bernoulli
+    masks; bf16, d = 128."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    causal: bool
+    window_left: int
+    per_head_mask: bool
+    d: int = 128
+    dtype: int = BF16
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.d)))
+
+    def kept_pairs(self) -> int:
+        """(row, key) pairs the band keeps (custom bits counted dense), per (batch, head)."""
+        i = np.arange(self.Sq)[:, None] + (self.Sk - self.Sq)
+        j = np.arange(self.Sk)[None, :]
+        keep = np.ones((self.Sq, self.Sk), bool)
+        if self.causal:
+            keep &= j <= i
+        if self.window_left >= 0:
+            keep &= j >= i - self.window_left
+        return int(keep.sum())
+
+    def flops(self) -> float:
+        """4*d per kept (row, key) pair: the two contractions over the band."""
+        return 4.0 * self.d * self.B * self.Hq * self.kept_pairs()
+
+    def make(self, seed):
+        """q [B,Hq,Sq,d], k and v [B,Hkv,Sk,d]; per-head mask bits [B,Hq,Sq,ceil(Sk/32)] or None."""
+        q, k, v = qkv(self.B, self.Hq, self.Hkv, self.Sk, self.d, self.dtype, seed)
+        q = q[:, :, self.Sk - self.Sq:].contiguous()
+        bits = None
+        if self.per_head_mask:
+            bits = pack_bits(bernoulli_mask(self.B * self.Hq, self.Sk, seed)[:, :self.Sq]).reshape(
+                self.B, self.Hq, self.Sq, -1)
+        return q, k, v, bits
+
+
+# Generalised-mode cases: a chunk of new queries against a long cache (GQA query-head pairs),
+# a causal sliding window over a long sequence, per-head custom masks.
+EX_WORKLOADS = {
+    "ex_sq128_sk32768_gqa8": ExWorkload("ex_sq128_sk32768_gqa8", 8, 32, 8, 128, 32768, True, -1, False),
+    "ex_window1024_S32768_gqa8": ExWorkload("ex_window1024_S32768_gqa8", 1, 32, 8, 32768, 32768, True, 1024, False),
+    "ex_perhead_mask_S4096_mha": ExWorkload("ex_perhead_mask_S4096_mha", 2, 16, 16, 4096, 4096, False, -1, True),
+}

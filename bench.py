@@ -427,6 +427,31 @@ def run_sweep(af, torch, dev, warmup=10, timed=50):
         rows[name] = row
         del t, qd, kd, vd, md, o, lse
         torch.cuda.empty_cache()
+    for name, xw in inp.EX_WORKLOADS.items():
+        # this library's extensions through attn_fwd_ex (not the pages' configurations)
+        q, k, v, bits = xw.make(2000 + xw.Sq % 1000)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        md = None if bits is None else torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(dev)
+        o = torch.empty_like(qd)
+        lse = torch.empty((xw.B, xw.Hq, xw.Sq), dtype=torch.float32, device=dev)
+
+        def xstep():
+            af.attn_fwd_ex(qd, kd, vd, o, lse, md, xw.per_head_mask, xw.causal, xw.window_left, -1, xw.scale)
+
+        ms = launch_times(torch, dev, xstep, warmup, timed, None)
+        af.attn_check()
+        med = statistics.median(ms)
+        p_tensor, _, _ = peaks()
+        ach = xw.flops() / (med / 1e3) / 1e12
+        rows[name] = {"ms_median": med, "ms_mean": statistics.mean(ms), "value": ach, "unit": "TFLOPS",
+                      "bound": "tensor", "achieved": ach, "achieved_unit": "TFLOP/s", "frac": ach / p_tensor,
+                      "B": xw.B, "Hq": xw.Hq, "Hkv": xw.Hkv, "Sq": xw.Sq, "Sk": xw.Sk, "d": xw.d,
+                      "causal": xw.causal, "window_left": xw.window_left, "per_head_mask": xw.per_head_mask,
+                      "flops": "4*d per kept (row, key) pair of the band, custom bits counted dense",
+                      "extension": "attn_fwd_ex case (not one of the pages' configurations)",
+                      "launches": timed * (3 if xw.per_head_mask else 1)}
+        del qd, kd, vd, md, o, lse
+        torch.cuda.empty_cache()
     for name, pw in inp.PACKED_WORKLOADS.items():
         # this library's extension: a packed variable-length batch, through attn_fwd_packed
         q, k, v, cu = pw.make(1000 + len(pw.lengths))

@@ -53,9 +53,12 @@
  *     on `stream`, whole MiB) made by the first custom-mask call on the stream
  *     and reused by every later one; a call that needs more frees the old block
  *     in stream order (cudaFreeAsync) and allocates a larger one.  Repeated calls
- *     of one shape therefore allocate nothing after the first.  The workspace is
- *     held until attn_release_workspace(stream) or process exit: release it
- *     before destroying a stream that has run custom masks.
+ *     of one shape therefore allocate nothing after the first.  Variable-length
+ *     batches (attn_fwd_ex with per-entry lengths or packed offsets) use the same
+ *     workspace for their work order, B*ceil(max Sq/256) ints after the mask
+ *     scratch (256-byte aligned).  The workspace is held until
+ *     attn_release_workspace(stream) or process exit: release it before
+ *     destroying a stream that has run custom masks or variable-length batches.
  *   - Errors: arguments are validated before any launch (ATTN_ERR_INVALID /
  *     ATTN_ERR_UNSUPPORTED, nothing launched); a failed launch returns
  *     ATTN_ERR_CUDA.  The work is asynchronous: a kernel that gives up on a

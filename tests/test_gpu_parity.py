@@ -191,3 +191,25 @@ def test_packed_workload_sampled_parity():
         o_ref, lse_ref = oracle_rows(qb, kb, vb, None, True, pw.scale, pw.dtype, rows)
         h, i = rows // s, rows % s
         assert_close(og[h, lo + i], lg[h, lo + i], o_ref, lse_ref, f"packed entry {b} (length {s})")
+
+
+@pytest.mark.parametrize("name", list(inp.EX_WORKLOADS))
+def test_ex_workloads_sampled_parity(name):
+    """The attn_fwd_ex cases of the benchmark's sweep, launched as bench.py launches them,
+    against the oracle's extended definition on a stratified row sample of every head."""
+    import attention_forward_07_gb300 as af
+    xw = inp.EX_WORKLOADS[name]
+    q, k, v, bits = xw.make(2000 + xw.Sq % 1000)
+    dev = "cuda"
+    md = None if bits is None else torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(dev)
+    o = torch.full((xw.B, xw.Hq, xw.Sq, xw.d), float("nan"), dtype=q.dtype, device=dev)
+    lse = torch.full((xw.B, xw.Hq, xw.Sq), float("nan"), dtype=torch.float32, device=dev)
+    af.attn_fwd_ex(q.to(dev), k.to(dev), v.to(dev), o, lse, md, xw.per_head_mask, xw.causal, xw.window_left, -1,
+                   xw.scale)
+    af.attn_check()
+    rows = stratified_rows(xw.B, xw.Hq, xw.Sq, seed=xw.Sq)
+    o_ref, lse_ref = oracle.attn_rows_ex(inp.as_u16(q), inp.as_u16(k), inp.as_u16(v), xw.dtype, rows, bits,
+                                         xw.per_head_mask, xw.causal, xw.window_left, -1, xw.scale)
+    og = o.float().cpu().numpy().astype(np.float64).reshape(-1, xw.d)
+    lg = lse.cpu().numpy().astype(np.float64).reshape(-1)
+    assert_close(og[rows], lg[rows], o_ref, lse_ref, name)
