@@ -16,21 +16,23 @@ pytestmark = pytest.mark.gpu
 N_CASES = 24
 
 
-def _config(seed):
-    g = np.random.default_rng(1000 + seed)
+def _config(seed, short_queries=False):
+    """short_queries: at most 128 queries and an even GQA group (query-head pairs), lengths and
+    packed layouts more often (the variable-length work order)."""
+    g = np.random.default_rng((5000 if short_queries else 1000) + seed)
     d = int(g.choice([64, 128]))
     dtype = int(g.choice([inp.F16, inp.BF16]))
     Hkv = int(g.choice([1, 2, 3]))
-    Hq = Hkv * int(g.choice([1, 2, 4]))
-    B = int(g.integers(1, 4))
-    Sq = int(g.integers(1, 420))
+    Hq = Hkv * int(g.choice([2, 4] if short_queries else [1, 2, 4]))
+    B = int(g.integers(1, 6 if short_queries else 4))
+    Sq = int(g.integers(1, 129 if short_queries else 420))
     Sk = int(g.integers(Sq, Sq + 300))
     causal = bool(g.random() < 0.5)
     wl = int(g.choice([-1, -1, int(g.integers(0, 200))]))
     wr = -1 if causal else int(g.choice([-1, -1, int(g.integers(0, 100))]))
     mask = str(g.choice(["none", "none", "shared", "head", "sparse"]))
-    packed = mask == "none" and bool(g.random() < 0.4)
-    lens = bool(g.random() < 0.4) or packed
+    packed = mask == "none" and bool(g.random() < (0.6 if short_queries else 0.4))
+    lens = bool(g.random() < (0.6 if short_queries else 0.4)) or packed
     lq = g.integers(0, Sq + 1, size=B).astype(np.int32) if lens else None
     lk = g.integers(0, Sk + 1, size=B).astype(np.int32) if lens else None
     return dict(d=d, dtype=dtype, Hkv=Hkv, Hq=Hq, B=B, Sq=Sq, Sk=Sk, causal=causal, wl=wl, wr=wr, mask=mask,
@@ -39,7 +41,15 @@ def _config(seed):
 
 @pytest.mark.parametrize("seed", range(N_CASES))
 def test_random_configuration(seed):
-    c = _config(seed)
+    _check(_config(seed), seed)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_short_query_configuration(seed):
+    _check(_config(seed, short_queries=True), 100 + seed)
+
+
+def _check(c, seed):
     B, Hq, Hkv, Sq, Sk, d, dtype = c["B"], c["Hq"], c["Hkv"], c["Sq"], c["Sk"], c["d"], c["dtype"]
     q, k, v = inp.qkv(B, Hq, Hkv, Sk, d, dtype, 77 * seed + 5)
     q = q[:, :, :Sq].contiguous()
