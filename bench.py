@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--e2e-buffers", type=int, default=2, help="device buffer sets in the end-to-end pipeline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
     return ap.parse_args(argv)
 
@@ -523,7 +524,7 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, max(3, min(K, 20)), world)
+        e2e = measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, max(3, min(K, 20)), world, args.e2e_buffers)
 
     mean_ms, med_ms = statistics.mean(per_launch_ms), statistics.median(per_launch_ms)
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
@@ -562,16 +563,15 @@ def run_ours(args):
     return 0
 
 
-def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world):
+def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world, nb=2):
     """Same metric through the public API with host buffers.  Every step copies its Q, K, V
     (and mask) from pinned host memory to the device, runs the forward, and copies O and LSE
-    back; steps are pipelined the way a serving loop runs them: double-buffered device
-    buffers, H2D copies on one stream, the forward on another, D2H copies on a third, so the
-    copies of neighbouring steps overlap the current step's kernel.  The timed region runs
+    back; steps are pipelined the way a serving loop runs them: nb sets of device buffers,
+    H2D copies on one stream, the forward on another, D2H copies on a third, so the copies
+    of neighbouring steps overlap the current step's kernel.  The timed region runs
     from before the first H2D copy to the end of the last D2H copy."""
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
     mh = None if bits is None else torch.from_numpy(bits.view(np.int32)).pin_memory()
-    nb = 2
     din = [[torch.empty_like(t, device=dev) for t in (qh, kh, vh)] + [None if mh is None else torch.empty_like(mh, device=dev)]
            for _ in range(nb)]
     dout = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(nb)]
@@ -587,7 +587,7 @@ def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world):
             b = i % nb
             with torch.cuda.stream(s_in):
                 if cmp_done[b] is not None:
-                    s_in.wait_event(cmp_done[b])  # inputs of step i-2 consumed
+                    s_in.wait_event(cmp_done[b])  # inputs of step i-nb consumed
                 for dst, src in zip(din[b], (qh, kh, vh, mh)):
                     if src is not None:
                         dst.copy_(src, non_blocking=True)
@@ -596,7 +596,7 @@ def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world):
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(in_done)
                 if out_done[b] is not None:
-                    s_cmp.wait_event(out_done[b])  # outputs of step i-2 copied out
+                    s_cmp.wait_event(out_done[b])  # outputs of step i-nb copied out
                 qd, kd, vd, md = din[b]
                 af.attn_fwd(qd, kd, vd, dout[b][0], dout[b][1], md, causal=w.causal, scale=w.scale, stream=s_cmp)
                 cmp_done[b] = ev()
@@ -608,7 +608,7 @@ def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world):
                 out_done[b] = ev()
                 out_done[b].record(s_out)
 
-    run(2)
+    run(nb)
     torch.cuda.synchronize(dev)
     barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -624,7 +624,7 @@ def measure_e2e(af, torch, dev, w, q, k, v, bits, o, lse, steps, world):
     d2h = o.numel() * o.element_size() + lse.numel() * 4
     return {"value": world * w.flops() / (ms / 1e3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
-            "pipelining": "double-buffered; H2D, forward and D2H on three streams"}
+            "pipelining": f"{nb} device buffer sets; H2D, forward and D2H on three streams"}
 
 
 def main(argv=None):
