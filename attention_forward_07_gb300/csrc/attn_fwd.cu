@@ -22,11 +22,11 @@
 //                exp2, row sum, write P back into TMEM as fp16/bf16, rescale the O row
 //                when the running max grew (the correction step), and at the end of the
 //                unit normalise O, store it and the LSE.
-// Work unit = (batch, query head, 256-row block).  Units of equal size and variable-length
-// batches come from a work queue per stream (an atomic counter the last CTA resets), the
-// latter in a longest-first order a one-CTA counting sort writes; causal units of uniform
-// lengths and custom-mask units are dealt in a fixed snake order, the heaviest blocks (most
-// key tiles) first.
+// Work unit = (batch, query head, 256-row block).  Units without a custom mask and
+// variable-length batches come from a work queue per stream (an atomic counter the last CTA
+// resets): causal ones longest first with a head's adjacent levels a few positions apart,
+// variable-length ones in the longest-first order a one-CTA counting sort writes.  Custom-mask
+// units and causal windows are dealt in a fixed snake order, the heaviest blocks first.
 // d = 64 keeps three S slots in TMEM shared by the two Q tiles, so a Q tile's next Q.K^T runs
 // while its softmax works on the current one.
 // Custom masks go through two small kernels first: the pre-pass ANDs the caller's words
@@ -260,10 +260,16 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 // Unit -> (batch, query head, 256-row block).
 // Variable-length batches (work queue): the pairs of p.order, longest first, the query heads
 // of a pair adjacent.
-// Causal: block index descending (the longest units first), the heads of a block adjacent; the
-// fixed snake walk deals them so that every CTA's total is close to the mean.
+// Causal from the work queue: block levels from the longest down, two levels at a time, the
+// (batch, head) pairs in blocks of CAUSAL_HEAD_BLOCK with a block's upper level just before
+// its lower one: a unit's next-lower neighbour of the same head is fetched ~32 positions
+// later, a fraction of a unit's time, so it finds the K/V tiles the first one read still in L2
+// without the two waiting on the same fetch.
+// Causal with the fixed walk (custom masks): block index descending, the heads of a block
+// adjacent; the snake deals them so that every CTA's total is close to the mean.
 // Otherwise: consecutive units walk the blocks and the query heads of one K/V head, so the
 // CTAs running at one time share K/V through L2.
+constexpr int CAUSAL_HEAD_BLOCK = 32;
 __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, bool pair, int& b, int& hq,
                                             int& qb) {
   if (pair) {
@@ -280,6 +286,22 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
     b = pair / p.nqb;
     qb = pair - b * p.nqb;
     hq = u - pi * p.Hq;
+  } else if (causal && p.dynamic) {
+    const int per = p.B * p.Hq, npl = p.nqb / 2;
+    int hidx;
+    if (u < npl * 2 * per) {
+      const int pl = u / (2 * per), r = u - pl * 2 * per;
+      const int blk = r / (2 * CAUSAL_HEAD_BLOCK), within = r - blk * 2 * CAUSAL_HEAD_BLOCK;
+      const int hb = min(CAUSAL_HEAD_BLOCK, per - blk * CAUSAL_HEAD_BLOCK);  // a last, partial block
+      const int lvl = within / hb;
+      hidx = blk * CAUSAL_HEAD_BLOCK + (within - lvl * hb);
+      qb = p.nqb - 1 - 2 * pl - lvl;
+    } else {
+      hidx = u - npl * 2 * per;  // an odd block count leaves block 0 on its own
+      qb = 0;
+    }
+    b = hidx / p.Hq;
+    hq = hidx - b * p.Hq;
   } else if (causal) {
     const int bh = u % (p.B * p.Hq);
     qb = p.nqb - 1 - u / (p.B * p.Hq);
@@ -1804,13 +1826,15 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // entry of a stream it has not seen: such a stream reports through the shared slot 0.
   StreamState* ss = stream_state(dev, a.stream, !noalloc);
   p.status_slot = ss ? ss->slot : 0;
-  // Units of equal size (no right bound on the keys, no custom mask) and variable-length
-  // batches are taken from the stream's work queue, so CTAs that finish early take more.
-  // Causal units of uniform lengths and custom-mask units keep the fixed snake walk over the
-  // longest-first order, which balances them better (measured).  The shared slot 0 may serve
-  // launches on several streams at once, so those keep the fixed walk too.
+  // Without a custom mask, units with no right bound on the keys, causal units (in the
+  // interleaved order of decode_unit) and variable-length batches are taken from the stream's
+  // work queue, so CTAs that finish early take more.  Custom-mask units and causal windows keep
+  // the fixed snake walk over the longest-first order, which balanced them better (measured).
+  // The shared slot 0 may serve launches on several streams at once, so those keep the fixed
+  // walk too.
   const bool varlen_batch = packed || a.seqlens_q || a.seqlens_k;
-  p.dynamic = (p.status_slot != 0 && (varlen_batch || (!a.mask_bits && p.er < 0))) ? 1 : 0;
+  p.dynamic = (p.status_slot != 0 &&
+               (varlen_batch || (!a.mask_bits && (p.er < 0 || (p.er == 0 && p.wl < 0))))) ? 1 : 0;
   // Variable-length batches with the work queue get a work order, longest units first.
   const bool with_order = varlen_batch && p.dynamic && 2ll * p.nkt + 1 <= 8192;
   const bool custom = mode == MASK_CUSTOM;
