@@ -1827,14 +1827,14 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   StreamState* ss = stream_state(dev, a.stream, !noalloc);
   p.status_slot = ss ? ss->slot : 0;
   // Without a custom mask, units with no right bound on the keys, causal units (in the
-  // interleaved order of decode_unit) and variable-length batches are taken from the stream's
-  // work queue, so CTAs that finish early take more.  Custom-mask units and causal windows keep
-  // the fixed snake walk over the longest-first order, which balanced them better (measured).
-  // The shared slot 0 may serve launches on several streams at once, so those keep the fixed
-  // walk too.
+  // interleaved order of decode_unit), windows of at least 1024 keys and variable-length
+  // batches are taken from the stream's work queue, so CTAs that finish early take more.
+  // Custom-mask units and narrower windows (a few key tiles per unit) keep the fixed snake
+  // walk over the longest-first order, which balanced them better (measured).  The shared
+  // slot 0 may serve launches on several streams at once, so those keep the fixed walk too.
   const bool varlen_batch = packed || a.seqlens_q || a.seqlens_k;
-  p.dynamic = (p.status_slot != 0 &&
-               (varlen_batch || (!a.mask_bits && (p.er < 0 || (p.er == 0 && p.wl < 0))))) ? 1 : 0;
+  const bool wide = p.wl < 0 || p.wl >= 1024;
+  p.dynamic = (p.status_slot != 0 && (varlen_batch || (!a.mask_bits && (p.er < 0 || (p.er == 0 && wide))))) ? 1 : 0;
   // Variable-length batches with the work queue get a work order, longest units first.
   const bool with_order = varlen_batch && p.dynamic && 2ll * p.nkt + 1 <= 8192;
   const bool custom = mode == MASK_CUSTOM;
