@@ -702,11 +702,23 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
               const uint32_t kbase = base + L::OFF_K + cur_kslot * L::KV_TILE_BYTES;
               // Q and K as K-major operands: 16 elements (32 bytes) per step inside a
               // 128-byte swizzle row, the next 64 elements one half-tile further.
+              if constexpr (D == 64) {
+                // d = 64 issues twice the instructions per flop: the descriptors are built
+                // once and stepped through their start-address field (address >> 4 in the
+                // low 14 bits; every offset here keeps it below 2^14)
+                const uint64_t qd = sdesc_sw128(qbase, 16, 1024), kd = sdesc_sw128(kbase, 16, 1024);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                mma_ss_elect(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                             ID_QK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                  mma_ss_elect(s_col, qd + off, kd + off, ID_QK, kk > 0 ? 1u : 0u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+                  mma_ss_elect(s_col, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                               ID_QK, kk > 0 ? 1u : 0u);
+                }
               }
               tc_commit_elect(bars + 8u * (L::B_STILE + new_slot));
               if (p.visited && lane == 0)
@@ -724,11 +736,19 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint8_t
               const uint32_t vbase = base + L::OFF_V + prev_vslot * L::KV_TILE_BYTES;
               // V tile as the MN-major B operand: 16 keys per step (2048 bytes), the two
               // 64-column halves of d are KV_TILE_BYTES/2 apart, 8-key groups 1024 apart.
+              if constexpr (D == 64) {
+                const uint64_t vd = sdesc_sw128(vbase, BN * 128, 1024);
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ts_elect(tmem + L::O_COL + t * L::O_STRIDE, p_col + kk * 8,
-                             sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
-                             (started || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / 16; ++kk)
+                  mma_ts_elect(tmem + L::O_COL + t * L::O_STRIDE, p_col + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4),
+                               ID_PV, (started || kk > 0) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                  mma_ts_elect(tmem + L::O_COL + t * L::O_STRIDE, p_col + kk * 8,
+                               sdesc_sw128(vbase + kk * 16 * 128, BN * 128, 1024), ID_PV,
+                               (started || kk > 0) ? 1u : 0u);
+              }
               started = true;
               if constexpr (L::RING) tc_commit_elect(bars + 8u * (L::B_OPV + t));
             }
