@@ -262,14 +262,14 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 // of a pair adjacent.
 // Causal from the work queue: block levels from the longest down, two levels at a time, the
 // (batch, head) pairs in blocks of CAUSAL_HEAD_BLOCK with a block's upper level just before
-// its lower one: a unit's next-lower neighbour of the same head is fetched ~32 positions
-// later, a fraction of a unit's time, so it finds the K/V tiles the first one read still in L2
-// without the two waiting on the same fetch.
+// its lower one: a unit's next-lower neighbour of the same head is fetched ~128 positions
+// later, under one wave of the persistent grid, so it finds the K/V tiles the first one read
+// still in L2 without the two waiting on the same fetch.
 // Causal with the fixed walk (custom masks): block index descending, the heads of a block
 // adjacent; the snake deals them so that every CTA's total is close to the mean.
 // Otherwise: consecutive units walk the blocks and the query heads of one K/V head, so the
 // CTAs running at one time share K/V through L2.
-constexpr int CAUSAL_HEAD_BLOCK = 32;
+constexpr int CAUSAL_HEAD_BLOCK = 128;
 __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, bool pair, int& b, int& hq,
                                             int& qb) {
   if (pair) {
