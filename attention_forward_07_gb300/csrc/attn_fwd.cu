@@ -24,9 +24,9 @@
 //                unit normalise O, store it and the LSE.
 // Work unit = (batch, query head, 256-row block).  Units without a custom mask and
 // variable-length batches come from a work queue per stream (an atomic counter the last CTA
-// resets): causal ones longest first with a head's adjacent levels a few positions apart,
-// variable-length ones in the longest-first order a one-CTA counting sort writes.  Custom-mask
-// units and causal windows are dealt in a fixed snake order, the heaviest blocks first.
+// resets): causal ones longest first (block level descending), variable-length ones in the
+// longest-first order a one-CTA counting sort writes.  Custom-mask units and windows narrower
+// than 1024 keys are dealt in a fixed snake order, the heaviest blocks first.
 // d = 64 keeps three S slots in TMEM shared by the two Q tiles, so a Q tile's next Q.K^T runs
 // while its softmax works on the current one.
 // Custom masks go through two small kernels first: the pre-pass ANDs the caller's words
@@ -260,16 +260,11 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 // Unit -> (batch, query head, 256-row block).
 // Variable-length batches (work queue): the pairs of p.order, longest first, the query heads
 // of a pair adjacent.
-// Causal from the work queue: block levels from the longest down, two levels at a time, the
-// (batch, head) pairs in blocks of CAUSAL_HEAD_BLOCK with a block's upper level just before
-// its lower one: a unit's next-lower neighbour of the same head is fetched ~128 positions
-// later, under one wave of the persistent grid, so it finds the K/V tiles the first one read
-// still in L2 without the two waiting on the same fetch.
-// Causal with the fixed walk (custom masks): block index descending, the heads of a block
-// adjacent; the snake deals them so that every CTA's total is close to the mean.
+// Causal: longest first — block index descending, the (batch, head) pairs of a block level
+// adjacent.  The work queue hands them out in that order; the fixed walk (custom masks) deals
+// them in a snake, so that every CTA's total is close to the mean.
 // Otherwise: consecutive units walk the blocks and the query heads of one K/V head, so the
 // CTAs running at one time share K/V through L2.
-constexpr int CAUSAL_HEAD_BLOCK = 128;
 __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, bool pair, int& b, int& hq,
                                             int& qb) {
   if (pair) {
@@ -286,22 +281,6 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
     b = pair / p.nqb;
     qb = pair - b * p.nqb;
     hq = u - pi * p.Hq;
-  } else if (causal && p.dynamic) {
-    const int per = p.B * p.Hq, npl = p.nqb / 2;
-    int hidx;
-    if (u < npl * 2 * per) {
-      const int pl = u / (2 * per), r = u - pl * 2 * per;
-      const int blk = r / (2 * CAUSAL_HEAD_BLOCK), within = r - blk * 2 * CAUSAL_HEAD_BLOCK;
-      const int hb = min(CAUSAL_HEAD_BLOCK, per - blk * CAUSAL_HEAD_BLOCK);  // a last, partial block
-      const int lvl = within / hb;
-      hidx = blk * CAUSAL_HEAD_BLOCK + (within - lvl * hb);
-      qb = p.nqb - 1 - 2 * pl - lvl;
-    } else {
-      hidx = u - npl * 2 * per;  // an odd block count leaves block 0 on its own
-      qb = 0;
-    }
-    b = hidx / p.Hq;
-    hq = hidx - b * p.Hq;
   } else if (causal) {
     const int bh = u % (p.B * p.Hq);
     qb = p.nqb - 1 - u / (p.B * p.Hq);
@@ -1846,9 +1825,9 @@ int fwd_impl(const attn_fwd_params_t& a, bool noalloc = false) {
   // entry of a stream it has not seen: such a stream reports through the shared slot 0.
   StreamState* ss = stream_state(dev, a.stream, !noalloc);
   p.status_slot = ss ? ss->slot : 0;
-  // Without a custom mask, units with no right bound on the keys, causal units (in the
-  // interleaved order of decode_unit), windows of at least 1024 keys and variable-length
-  // batches are taken from the stream's work queue, so CTAs that finish early take more.
+  // Without a custom mask, units with no right bound on the keys, causal units (longest
+  // first), windows of at least 1024 keys and variable-length batches are taken from the
+  // stream's work queue, so CTAs that finish early take more.
   // Custom-mask units and narrower windows (a few key tiles per unit) keep the fixed snake
   // walk over the longest-first order, which balanced them better (measured).  The shared
   // slot 0 may serve launches on several streams at once, so those keep the fixed walk too.

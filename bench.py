@@ -296,9 +296,9 @@ def run_reference(args):
 MEASURED_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, captured at
     # full size (one launch, metrics-only, 1 pass) on the kernel with this source hash
-    "b8dda7e78ebf": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1789.31e6 + 236.78e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.44e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_block90": 36.92e6 + 0.02e6},
+    "bfe887a39b8f": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1823.68e6 + 236.44e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.46e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_block90": 36.91e6 + 0.01e6},
 }
 
 
