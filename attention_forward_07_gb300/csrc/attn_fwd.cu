@@ -263,10 +263,13 @@ __device__ __forceinline__ int unit_at(int k, int num_units) {
 // Causal: longest first — block index descending, the (batch, head) pairs of a block level
 // adjacent.  The work queue hands them out in that order; the fixed walk (custom masks) deals
 // them in a snake, so that every CTA's total is close to the mean.
+// Custom masks without causal: block level by level from block 0.  Row compaction packs a mask
+// row block's kept 16-row blocks into its first units, so this is longest first there too, and
+// the snake does not deal the empty units of a sparse mask to every other CTA.
 // Otherwise: consecutive units walk the blocks and the query heads of one K/V head, so the
 // CTAs running at one time share K/V through L2.
-__device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, bool pair, int& b, int& hq,
-                                            int& qb) {
+__device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal, bool pair, bool custom, int& b,
+                                            int& hq, int& qb) {
   if (pair) {
     // (entry, block) pairs in the work order or in index order, then the head pairs of
     // consecutive K/V heads (an even group size keeps a pair inside one group)
@@ -281,9 +284,9 @@ __device__ __forceinline__ void decode_unit(int u, const Params& p, bool causal,
     b = pair / p.nqb;
     qb = pair - b * p.nqb;
     hq = u - pi * p.Hq;
-  } else if (causal) {
-    const int bh = u % (p.B * p.Hq);
-    qb = p.nqb - 1 - u / (p.B * p.Hq);
+  } else if (causal || custom) {
+    const int bh = u % (p.B * p.Hq), level = u / (p.B * p.Hq);
+    qb = causal ? p.nqb - 1 - level : level;
     b = bh / p.Hq;
     hq = bh % p.Hq;
   } else {
@@ -393,7 +396,7 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
       break;
     }
     int b, hq, qb;
-    decode_unit(u, p, causal, pair, b, hq, qb);
+    decode_unit(u, p, causal, pair, MODE == MASK_CUSTOM, b, hq, qb);
     const int hkv = hq / p.g;
     const int row0 = qb * UNIT_ROWS;
     const int mb = p.mask_heads > 1 ? b * p.Hq + hq : b;  // custom-mask row block
@@ -1176,8 +1179,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Custom masks: the set-up above overlapped the mask kernels (dependent launch); their
-  // words, flags and slot lists are read only after this point.
   // Custom masks and variable-length work orders: the set-up above overlapped the kernels
   // that write them (dependent launch); they are read only after this point.
   if (MODE == MASK_CUSTOM || p.order) grid_dependency_wait();
