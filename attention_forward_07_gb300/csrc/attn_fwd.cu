@@ -1237,7 +1237,7 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
 __global__ void __launch_bounds__(BM) mask_prepass_kernel(const uint32_t* __restrict__ mask,
                                                           uint32_t* __restrict__ words4,
                                                           uint8_t* __restrict__ flags16, Params p,
-                                                          int nmb) {
+                                                          int nmb, int write_words) {
   // One CTA per (mask row block, 128 query rows, key tile), one thread per query row: every
   // thread's four words are loaded together; each half-warp's OR is the emptiness flag of
   // one (16-row block, key tile) pair.
@@ -1271,7 +1271,7 @@ __global__ void __launch_bounds__(BM) mask_prepass_kernel(const uint32_t* __rest
       x[w] &= bit_range(klo - gw * 32, khi - gw * 32);
       any |= x[w];
     }
-    *reinterpret_cast<uint4*>(dst + kt * 4) = make_uint4(x[0], x[1], x[2], x[3]);
+    if (write_words) *reinterpret_cast<uint4*>(dst + kt * 4) = make_uint4(x[0], x[1], x[2], x[3]);
   }
   const uint32_t bits = __ballot_sync(0xffffffffu, any != 0u);
   if ((threadIdx.x & 31) == 0) {
@@ -1663,7 +1663,12 @@ int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream
       attr_set.fetch_or(bit);
     }
   }
-  mask_prepass_kernel<<<(unsigned)blocks, BM, 0, st>>>(mask_bits, words4, flags16, p, nmb);
+  // When no bound applies (no band or causal bound, no per-entry lengths) and the key count is
+  // a multiple of the key tile, the padded words equal the caller's words byte for byte: the
+  // kernel then reads those (through 16-byte-aligned rows), and the pre-pass only flags.
+  const bool words_in_place = p.Sk % BN == 0 && p.W == 4 * p.nkt && p.wl < 0 && p.er < 0 && !p.lens_q &&
+                              !p.lens_k && !p.cu_q && (reinterpret_cast<uintptr_t>(mask_bits) & 15u) == 0;
+  mask_prepass_kernel<<<(unsigned)blocks, BM, 0, st>>>(mask_bits, words4, flags16, p, nmb, words_in_place ? 0 : 1);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   {
     cudaLaunchConfig_t cfg = {};
@@ -1680,8 +1685,9 @@ int prepare_mask(Params& p, const uint32_t* mask_bits, void* scratch, cudaStream
                            p.nqt, nslots) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
-  int rc = make_mask_map(&p.tm_m, words4, 4 * p.nkt, p.Sq, nmb, 16);
-  return rc != ATTN_OK ? rc : make_mask_map(&p.tm_m256, words4, 4 * p.nkt, p.Sq, nmb, UNIT_ROWS);
+  const uint32_t* words = words_in_place ? mask_bits : words4;
+  int rc = make_mask_map(&p.tm_m, words, 4 * p.nkt, p.Sq, nmb, 16);
+  return rc != ATTN_OK ? rc : make_mask_map(&p.tm_m256, words, 4 * p.nkt, p.Sq, nmb, UNIT_ROWS);
 }
 
 template <int D, bool BF16, int MODE>

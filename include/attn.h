@@ -40,7 +40,10 @@
  *     (device, stream) that has run a custom mask, one workspace.  Without a
  *     custom mask nothing is allocated.  With one, a pre-pass kernel writes the
  *     kept-bit words (mask AND causal AND the key bound, padded to whole
- *     128-column tiles) and an emptiness map per (16-row block, 128-column tile),
+ *     128-column tiles; when no bound applies, the key count is a multiple of
+ *     128 and mask_bits is 16-byte aligned those equal mask_bits, which the
+ *     attention kernel then reads in place) and an emptiness map per (16-row
+ *     block, 128-column tile),
  *     and a compaction kernel lists, per mask row block, the 16-row blocks that
  *     keep anything: the attention kernel computes only those, packed eight to a
  *     128-row tile, and writes O = 0, LSE = -inf for the rows of the others
