@@ -296,9 +296,9 @@ def run_reference(args):
 MEASURED_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, captured at
     # full size (one launch, metrics-only, 1 pass) on the kernel with this source hash
-    "e59a07514312": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1804.22e6 + 236.57e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.47e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_block90": 36.91e6 + 0.01e6},
+    "d6bbe6d901dd": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1815.73e6 + 236.65e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.49e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_block90": 36.91e6 + 0.00e6},
 }
 
 
