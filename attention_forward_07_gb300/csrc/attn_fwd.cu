@@ -30,15 +30,17 @@
 // d = 64 keeps three S slots in TMEM shared by the two Q tiles, so a Q tile's next Q.K^T runs
 // while its softmax works on the current one.
 // Custom masks go through two small kernels first: the pre-pass ANDs the caller's words
-// with the causal / window / length bounds into whole-tile words and flags each (16-row
-// block, key tile) pair that keeps anything; the compaction lists the 16-row blocks that
-// keep anything.  A unit then computes the next sixteen listed blocks as its two Q tiles
-// (gathered block by block, or loaded whole when they are its own rows) and writes O = 0,
-// LSE = -inf for the rows of its own blocks that keep nothing.  Both kernels let the next
+// with the causal / window / length bounds into whole-tile words (or, when no bound applies
+// and the words already fill whole tiles, leaves the kernel to read the caller's) and flags
+// each (16-row block, key tile) pair that keeps anything; the compaction lists the 16-row
+// blocks that keep anything.  A unit then computes the next sixteen listed blocks as its two
+// Q tiles (gathered block by block, or loaded whole when they are its own rows) and writes
+// O = 0, LSE = -inf for the rows of its own blocks that keep nothing.  Both kernels let the next
 // grid start early (programmatic dependent launch) and the attention kernel waits for
 // their output with griddepcontrol.wait.
 // Every barrier wait is bounded: a wait that runs out sets a shared abort flag and the
-// device status word, every role drains what it has in flight and the CTA returns.
+// launch's per-stream status word, every role drains what it has in flight and the CTA
+// returns.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
