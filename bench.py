@@ -54,6 +54,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--e2e-buffers", type=int, default=2, help="device buffer sets in the end-to-end pipeline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
+    ap.add_argument("--sweep-only", default=None, metavar="NAME",
+                    help="time one workload of the sweep (the pages' or an extension) with --warmup / --steps "
+                         "launches and print its row as one JSON line instead of the bench line")
     return ap.parse_args(argv)
 
 
@@ -402,12 +405,15 @@ def skip_counts(af, torch, dev, w, tensors):
     return out
 
 
-def run_sweep(af, torch, dev, warmup=10, timed=50):
-    """Every workload of the pages' benchmarks, timed like the headline one."""
+def run_sweep(af, torch, dev, warmup=10, timed=50, names=None):
+    """Every workload of the pages' benchmarks, timed like the headline one (only `names` when
+    given)."""
     from attention_forward_07_gb300 import inputs as inp
     rows = {}
     fbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for idx, (name, w) in enumerate(inp.WORKLOADS.items()):
+        if names is not None and name not in names:
+            continue
         (_, _, _, bits), t = device_inputs(torch, dev, w, w.seed(idx))
         qd, kd, vd, md, o, lse = t
 
@@ -430,6 +436,8 @@ def run_sweep(af, torch, dev, warmup=10, timed=50):
         torch.cuda.empty_cache()
     for name, xw in inp.EX_WORKLOADS.items():
         # this library's extensions through attn_fwd_ex (not the pages' configurations)
+        if names is not None and name not in names:
+            continue
         q, k, v, bits = xw.make(2000 + xw.Sq % 1000)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         md = None if bits is None else torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(dev)
@@ -455,6 +463,8 @@ def run_sweep(af, torch, dev, warmup=10, timed=50):
         torch.cuda.empty_cache()
     for name, pw in inp.PACKED_WORKLOADS.items():
         # this library's extension: a packed variable-length batch, through attn_fwd_packed
+        if names is not None and name not in names:
+            continue
         q, k, v, cu = pw.make(1000 + len(pw.lengths))
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         cud = torch.from_numpy(cu).to(dev)
@@ -493,6 +503,15 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     import attention_forward_07_gb300 as af
     af.library()  # fail loudly here if the CUDA library is missing
+    if args.sweep_only:
+        from attention_forward_07_gb300 import inputs as inp
+        known = set(inp.WORKLOADS) | set(inp.EX_WORKLOADS) | set(inp.PACKED_WORKLOADS)
+        if args.sweep_only not in known:
+            raise SystemExit(f"--sweep-only: unknown workload {args.sweep_only!r}")
+        rows = run_sweep(af, torch, dev, warmup=args.warmup, timed=args.steps, names={args.sweep_only})
+        if rank == 0:
+            print(json.dumps({"workload": args.sweep_only, "kernel": kernel_hash(), **rows[args.sweep_only]}))
+        return 0
     w, idx = workload(args.workload, args.batch)
     seed = replica_seed(w.seed(idx), rank)
     (q, k, v, bits), t = device_inputs(torch, dev, w, seed)
