@@ -476,7 +476,13 @@ __device__ __forceinline__ void load_role(const Params& p, uint32_t base, uint8_
     const int jbeg = jhi[0] < 0 ? jlo[1] : (jhi[1] < 0 ? jlo[0] : min(jlo[0], jlo[1]));
     const int jend = max(jhi[0], jhi[1]) + 1;
     uint32_t f0 = 0, f1 = 0;  // bit (j % 32): Q tile 0 / 1 has a kept entry in key tile j
-    for (int j = jbeg; j < jend; ++j) {
+    // Causal: odd block levels walk their key tiles from the diagonal down.  Longest first, a
+    // head's next-lower level starts about when its current one ends, so it begins on the K/V
+    // tiles that level read last (still in L2) rather than on its oldest ones.  The online
+    // softmax does not depend on the order of the key tiles.
+    const bool down = MODE == MASK_CAUSAL && (qb & 1);
+    for (int jj = jbeg; jj < jend; ++jj) {
+      const int j = down ? jend - 1 - (jj - jbeg) : jj;
       bool a0 = j >= jlo[0] && j <= jhi[0];
       bool a1 = j >= jlo[1] && j <= jhi[1];
       if constexpr (MODE == MASK_CUSTOM) {

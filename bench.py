@@ -299,8 +299,8 @@ def run_reference(args):
 MEASURED_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one attention-kernel launch, captured at
     # full size (one launch, metrics-only, 1 pass) on the kernel with this source hash
-    "d6bbe6d901dd": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1815.73e6 + 236.65e6,
-                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.49e6,
+    "bf31ac772055": {"B4_Hq32_Hkv8_S8192_d128_causal_none": 1338.56e6 + 236.14e6,
+                     "B16_Hq16_Hkv16_S512_d64_full_bernoulli": 50.94e6 + 0.26e6,
                      "B16_Hq16_Hkv16_S512_d64_full_block90": 36.91e6 + 0.00e6},
 }
 

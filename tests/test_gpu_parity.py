@@ -88,7 +88,11 @@ def test_causal_equals_lower_triangular_mask():
     tri = inp.pack_bits(torch.tril(torch.ones((S, S), dtype=torch.bool)).expand(B, S, S))
     a = run_cuda(q, k, v, None, True, 0.09)
     b = run_cuda(q, k, v, tri, False, 0.09)
-    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=2e-3)
+    # The causal path walks the key tiles of odd block levels from the diagonal down, the mask
+    # path from key 0 up.  The order changes the fp32 sums and the exponent base each row
+    # settles on (so P rounds to bf16 differently): absolute differences of order 1e-3, and an
+    # output may then round to the neighbouring bf16 value (one step = 2^-7 of its magnitude).
+    np.testing.assert_allclose(a[0], b[0], rtol=2.0 ** -7, atol=2e-3)
     np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-4)
 
 
